@@ -1,0 +1,466 @@
+"""Throughput of the DeepSeek-V3-shaped MoE layer forward on GB300.
+
+One step = one moe_forward call (router linear, gate, dispatch, token gather, gate/up
+GEMM with SwiGLU, down GEMM, combine; shared expert included) on one batch of synthetic
+tokens with device-resident random-init weights.  Default workload: DeepSeek-V3 shape,
+decode T=128 (d=7168, 256 routed experts + 1 shared, I=2048, top-8 of 8 groups keep 4);
+the prefill shape (T=8192, Zipf-skewed routing) is measured in the same run and reported
+under "prefill".  Timing: CUDA events on the launch stream, W untimed warm-up steps, the L2
+flushed (256 MB write) before every timed step, steps summed between their own events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs N independent replicas (the layer has no exchange step), one per rank under
+torchrun; value = tokens of all ranks / max over ranks of the timed time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from deepseek_moe_layer_gb300 import binding, inputs  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (DSv3 shape, T=128 & T=8192); % of HBM/tensor roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic (read + write bytes per launch) of the dominant kernel from an ncu capture,
+# keyed by workload, with the hash of the GEMM sources it was taken on; stale -> null.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "deepseek_moe_layer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+        except Exception:
+            uuid = str(dev.index or 0)
+        self.uuid = uuid
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = np.array([r[0] for r in rows])
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3][1:5])
+                          if v.lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(r[1] for r in rows)),
+                "power_w_max": float(max(r[2] for r in rows)), "samples": len(rows),
+                "reasons": reasons}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def algorithmic(w, counts):
+    """Algorithmic bytes and FLOPs of one forward, from the measured expert loads."""
+    T, d, I, E, K = w.T, w.d, w.I, w.E, w.top_k
+    P = T * K
+    hit = int((counts > 0).sum())
+    nsh = 1 if w.shared else 0
+    rows = P + (T if w.shared else 0)
+    if w.bits == 16:
+        wmat = I * d * 2                     # bytes of one [I, d] bf16 matrix
+    else:
+        wmat = I * d // 2 + 2 * (I * d // 64) * 2
+    shmat = I * d * 2
+    gate_up_w = hit * 2 * wmat + nsh * 2 * shmat
+    down_w = hit * wmat + nsh * shmat
+    out = {
+        "experts_hit": hit,
+        "gate_up_bytes": gate_up_w + rows * d * 2 + rows * I * 2,
+        "down_bytes": down_w + rows * I * 2 + rows * d * 2,
+        "gate_up_flops": 2.0 * rows * d * 2 * I,
+        "down_flops": 2.0 * rows * I * d,
+        "router_flops": 2.0 * T * d * E,
+        "layer_bytes": gate_up_w + down_w + E * d * 2 + 2 * T * d * 2,
+    }
+    out["layer_flops"] = out["gate_up_flops"] + out["down_flops"] + out["router_flops"]
+    return out
+
+
+def make_layer(w, data):
+    return binding.MoELayer(data["w_router"], data["bias"], data["experts"], data["shared"],
+                            w.top_k, w.n_group, w.topk_group, w.norm_topk_prob,
+                            w.routed_scaling_factor, data["logit_offset"])
+
+
+def time_layer(w, data, steps, warmup, dev, sampler=None):
+    """Device time of `steps` forwards (each preceded by an L2 flush), per-phase times."""
+    layer = make_layer(w, data)
+    x = data["x"]
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    y = torch.empty(w.T, w.d, dtype=torch.bfloat16, device=dev)
+    for _ in range(warmup):
+        layer(x, y=y)
+    torch.cuda.synchronize(dev)
+    binding.device_status()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(steps)]
+    if torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    for s in range(steps):
+        flush.zero_()
+        binding.set_phase_events(evs[s])
+        layer(x, y=y)
+    binding.set_phase_events(None)
+    torch.cuda.synchronize(dev)
+    if torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    binding.device_status()
+    per_step = np.array([evs[s][0].elapsed_time(evs[s][7]) for s in range(steps)])
+    phases = {name: float(np.mean([evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)]))
+              for i, name in enumerate(binding.PHASES)}
+    _, inds, _, _ = layer(x, want_intermediates=True)
+    torch.cuda.synchronize(dev)
+    counts = np.bincount(inds.cpu().numpy().reshape(-1), minlength=w.E)
+    return dict(total_ms=float(per_step.sum()), ms=float(per_step.mean()), phases=phases,
+                counts=counts, launches=7 * steps)
+
+
+def time_e2e(w, data, steps, warmup, dev):
+    """Same forward through the public API with the tokens in pinned host memory: each
+    step copies x host->device, runs the layer, copies y device->host."""
+    layer = make_layer(w, data)
+    xh = data["x"].cpu().pin_memory()
+    yh = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(data["x"])
+    yd = torch.empty(w.T, w.d, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        xd.copy_(xh, non_blocking=True)
+        layer(xd, y=yd)
+        yh.copy_(yd, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b)
+    return dict(ms=ms, h2d=xh.numel() * 2, d2h=yh.numel() * 2)
+
+
+def roofline(kind, achieved_per_s, peaks, sustained, traffic=None):
+    if kind == "hbm":
+        peak = peaks["hbm_gbs"]
+        a = achieved_per_s / 1e9
+        unit = "GB/s"
+    else:
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        a = achieved_per_s / 1e12
+        unit = "TFLOP/s"
+    return {"bound": kind, "achieved": round(a, 1), "peak": peak, "unit": unit,
+            "frac": round(a / peak, 4), "traffic": traffic}
+
+
+def kernel_roofline(w, t, alg, peaks, src):
+    """Roofline of the dominant kernel (the gate/up GEMM): HBM-bound when its bytes at
+    peak bandwidth take longer than its FLOPs at peak tensor rate, else tensor-bound."""
+    sec = t["phases"]["gate_up"] / 1e3
+    t_hbm = alg["gate_up_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg["gate_up_flops"] / (peaks["bf16_tflops_sustained"] * 1e12)
+    tr = NCU_TRAFFIC.get(w.name)
+    traffic = tr["bytes"] if tr and tr.get("src") == src else None
+    if t_hbm >= t_tc:
+        r = roofline("hbm", alg["gate_up_bytes"] / sec, peaks, True, traffic)
+        r["algorithmic"] = alg["gate_up_bytes"]
+    else:
+        r = roofline("tensor", alg["gate_up_flops"] / sec, peaks, True, traffic)
+        r["algorithmic"] = alg["gate_up_flops"]
+    r["kernel"] = "moe_gemm_kernel<kGateUp> (gate/up GEMM + SwiGLU)"
+    r["ms"] = round(t["phases"]["gate_up"], 4)
+    return r
+
+
+def layer_roofline(alg, ms, peaks):
+    sec = ms / 1e3
+    t_hbm = alg["layer_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg["layer_flops"] / (peaks["bf16_tflops_sustained"] * 1e12)
+    if t_hbm >= t_tc:
+        return roofline("hbm", alg["layer_bytes"] / sec, peaks, True)
+    return roofline("tensor", alg["layer_flops"] / sec, peaks, True)
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle timing (baseline and the reference arm)
+# ---------------------------------------------------------------------------------------
+
+def _bits(t):
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_inputs(w, data, rows):
+    """Host copies of what the oracle needs for `rows` (only the experts they route to)."""
+    import oracle
+    xb = _bits(data["x"][torch.as_tensor(rows, device=data["x"].device)])
+    wr = _bits(data["w_router"])
+    off = None if data["logit_offset"] is None else data["logit_offset"].cpu().numpy()
+    bias = data["bias"].cpu().numpy()
+    lg = oracle.router_logits(xb, wr, off)
+    inds, _ = oracle.route(lg, bias, w.top_k, w.n_group, w.topk_group, w.norm_topk_prob,
+                           w.routed_scaling_factor)
+    used = np.unique(inds)
+    idx = torch.as_tensor(used, device=data["w_router"].device)
+    ex = {"bits": data["experts"]["bits"]}
+    for k, v in data["experts"].items():
+        if isinstance(v, torch.Tensor):
+            t = v.index_select(0, idx)
+            ex[k] = t.cpu().numpy().view(np.uint32) if t.dtype == torch.int32 else _bits(t)
+    remap = np.full(w.E, -1, np.int64)
+    remap[used] = np.arange(len(used))
+    sh = None if data["shared"] is None else {k: _bits(data["shared"][k])
+                                              for k in ("gate", "up", "down")}
+    return dict(xb=xb, wr=wr, off=off, bias=bias, ex=ex, sh=sh, remap=remap)
+
+
+def oracle_step(w, h):
+    """One timed oracle pass over the sampled tokens (router linear -> gate -> dispatch ->
+    dense per-token layer), exactly as the oracle stands."""
+    import oracle
+    lg = oracle.router_logits(h["xb"], h["wr"], h["off"])
+    inds, scores = oracle.route(lg, h["bias"], w.top_k, w.n_group, w.topk_group,
+                                w.norm_topk_prob, w.routed_scaling_factor)
+    E_used = int(h["remap"].max()) + 1
+    loc = h["remap"][inds].astype(np.int32)
+    oracle.permute(loc, E_used)
+    return oracle.moe_layer(h["xb"], loc, scores, h["ex"], h["sh"])
+
+
+def cpu_baseline(w, data, target_s=10.0):
+    import oracle
+    n = max(4, oracle.num_threads())
+    rows = np.arange(min(w.T, n))
+    h = oracle_inputs(w, data, rows)
+    t0 = time.perf_counter()
+    oracle_step(w, h)
+    dt = time.perf_counter() - t0
+    reps = max(1, min(int(target_s / max(dt, 1e-3)), 20))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(w, h)
+    dt = time.perf_counter() - t0
+    return {"value": round(len(rows) * reps / dt, 3), "unit": "tokens/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} tokens of {w.name} x {reps} passes (router linear, gate, "
+                      f"dispatch, dense per-token expert loop incl. shared expert), "
+                      f"{dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------------------
+
+def workload_data(name, dev, base=None):
+    w = inputs.WORKLOADS[name]
+    if base is None:
+        return w, inputs.gen_layer(w, dev, seed=0)
+    data = dict(base)
+    data["x"] = inputs.gen_tokens(w, dev, seed=0)
+    data["logit_offset"] = inputs.zipf_offsets(w.E, dev, 0) if w.zipf else None
+    return w, data
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    src = kernel_source_hash()
+
+    w, data = workload_data(args.workload, dev)
+    sampler = ClockSampler(dev)
+    with sampler:
+        t = time_layer(w, data, args.steps, args.warmup, dev)
+    clocks = sampler.summary()
+    e2e = time_e2e(w, data, args.steps, args.warmup, dev)
+    alg = algorithmic(w, t["counts"])
+
+    pre = None
+    if args.prefill and not args.workload.startswith("tiny"):
+        wp, dp = workload_data(args.prefill, dev, base=data)
+        tp = time_layer(wp, dp, args.steps, args.warmup, dev)
+        algp = algorithmic(wp, tp["counts"])
+        pre = {"workload": wp.name, "T": wp.T, "value": round(wp.T / (tp["ms"] / 1e3), 1),
+               "unit": "tokens/s", "ms_per_step": round(tp["ms"], 4),
+               "phases_ms": {k: round(v, 4) for k, v in tp["phases"].items()},
+               "experts_hit": algp["experts_hit"], "max_expert_load": int(tp["counts"].max()),
+               "roofline": kernel_roofline(wp, tp, algp, peaks, src),
+               "layer_roofline": layer_roofline(algp, tp["ms"], peaks)}
+        del dp
+
+    # aggregate over ranks: tokens of all ranks / max time
+    tot = torch.tensor([t["total_ms"], e2e["ms"]], dtype=torch.float64)
+    if ws > 1:
+        tot = tot.to(dev)
+        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
+        tot = tot.cpu()
+    total_ms, e2e_ms = float(tot[0]), float(tot[1])
+    value = ws * args.steps * w.T / (total_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1/fan_in) random-init weights, N(0,1) tokens",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "I": w.I,
+                   "top_k": w.top_k, "n_group": w.n_group, "topk_group": w.topk_group,
+                   "shared_experts": 1 if w.shared else 0, "expert_bits": w.bits,
+                   "parallelism": f"replicas x{ws}",
+                   "l2": "L2 flushed (256 MB write) before every timed step; expert "
+                         "weights per step exceed L2"},
+        "roofline": kernel_roofline(w, t, alg, peaks, src),
+        "layer_roofline": layer_roofline(alg, t["ms"], peaks),
+        "peaks_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+        "phases_ms": {k: round(v, 4) for k, v in t["phases"].items()},
+        "experts_hit": alg["experts_hit"],
+        "clocks": clocks,
+        "e2e": {"value": round(ws * args.steps * w.T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": t["launches"],
+        "kernel_src": src,
+    }
+    if pre is not None:
+        line["prefill"] = pre
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, data)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    dev = torch.device(f"cuda:{local}") if torch.cuda.is_available() else torch.device("cpu")
+    w, data = workload_data(args.workload, dev)
+    n = max(4, oracle.num_threads())
+    rows = np.arange(min(w.T, n))
+    h = oracle_inputs(w, data, rows)
+    for _ in range(args.warmup):
+        oracle_step(w, h)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, h)
+    dt = time.perf_counter() - t0
+    v = len(rows) * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64",
+        "data": "synthetic: seeded N(0,1/fan_in) random-init weights, N(0,1) tokens",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "I": w.I,
+                   "top_k": w.top_k, "n_group": w.n_group, "topk_group": w.topk_group,
+                   "shared_experts": 1 if w.shared else 0, "expert_bits": w.bits},
+        "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "kind": "oracle",
+                         "cores": oracle.num_threads(),
+                         "sample": f"each step: {len(rows)} tokens of {w.name} through the "
+                                   f"CPU oracle (router linear, gate, dispatch, dense "
+                                   f"per-token experts + shared)"},
+        "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dsv3_T128", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--prefill", default="dsv3_T8192_zipf")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.prefill in ("", "none"):
+        args.prefill = None
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

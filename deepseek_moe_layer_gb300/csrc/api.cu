@@ -1,0 +1,530 @@
+// api.cu -- the C ABI declared in include/moe_gb300.h: argument checks (all on the host,
+// before any CUDA call, so a rejected call touches nothing), workspace layout, and the
+// launch sequence of the layer on one stream.
+//
+// Source of the call contract: "feat(engine): E1 DeepSeek-style MoE gate (sigmoid, group
+// top-k, bias) (#108)", sections "API" (precomputed logits [..., E], required bias [E],
+// outputs inds / scores [..., K]) and the review's "What looks solid" 4 (outputs left
+// unchanged on failure) and "Findings" L1/L2 with the author's reply (the validation
+// matrix: null arguments, top_k == 0, top_k > E, E % n_group != 0, topk_group out of
+// [1, n_group], n_group > 1 with fewer than two experts per group, bias rank != 1).
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/moe_gb300.h"
+#include "launch.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+    return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+#define MOE_CHECK(cond, ...)                                  \
+    do {                                                      \
+        if (!(cond)) return fail(MOE_ERR_INVALID, __VA_ARGS__); \
+    } while (0)
+
+#define MOE_CUDA(call, where)                          \
+    do {                                               \
+        cudaError_t e_ = (call);                       \
+        if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+    } while (0)
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxPhaseEvents = 8;
+
+cudaEvent_t g_phase_ev[kMaxPhaseEvents];
+int g_phase_n = 0;
+
+cudaError_t phase(int i, cudaStream_t s) {
+    return i < g_phase_n ? cudaEventRecord(g_phase_ev[i], s) : cudaSuccess;
+}
+constexpr int kMaxTopK = 32;
+constexpr int kMaxGroups = 32;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// The current device must be an sm_103 part (GB300).  Checked once per device.
+int check_device() {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(MOE_ERR_NODEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    static int checked[64] = {0};
+    if (dev >= 0 && dev < 64 && checked[dev] == 1) return MOE_OK;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+        return fail(MOE_ERR_NODEVICE, "device %d is sm_%d%d; this library is built for sm_103a",
+                    dev, major, minor);
+    if (dev >= 0 && dev < 64) checked[dev] = 1;
+    return MOE_OK;
+}
+
+int check_route_params(int32_t E, const moe_route_params_t* p) {
+    MOE_CHECK(p, "params is NULL");
+    MOE_CHECK(E >= 1 && E <= kMaxExperts, "E = %d outside [1, %d]", E, kMaxExperts);
+    MOE_CHECK(p->top_k >= 1, "top_k = %d < 1", p->top_k);
+    MOE_CHECK(p->top_k <= E, "top_k = %d > E = %d", p->top_k, E);
+    MOE_CHECK(p->top_k <= kMaxTopK, "top_k = %d > %d", p->top_k, kMaxTopK);
+    MOE_CHECK(p->n_group >= 1, "n_group = %d < 1", p->n_group);
+    MOE_CHECK(p->n_group <= kMaxGroups, "n_group = %d > %d", p->n_group, kMaxGroups);
+    MOE_CHECK(E % p->n_group == 0, "E = %d not divisible by n_group = %d", E, p->n_group);
+    MOE_CHECK(p->topk_group >= 1 && p->topk_group <= p->n_group,
+              "topk_group = %d outside [1, n_group = %d]", p->topk_group, p->n_group);
+    MOE_CHECK(p->n_group == 1 || E / p->n_group >= 2,
+              "n_group = %d leaves %d expert(s) per group; the group score needs 2", p->n_group,
+              E / p->n_group);
+    return MOE_OK;
+}
+
+int check_weights(const moe_expert_weights_t* w, const char* what, int shared) {
+    MOE_CHECK(w, "%s weights are NULL", what);
+    MOE_CHECK(w->bits == 16 || w->bits == 4, "%s weights: bits = %d (16 or 4)", what, w->bits);
+    MOE_CHECK(!shared || w->bits == 16, "%s weights must be bf16 (bits 16)", what);
+    MOE_CHECK(w->gate && w->up && w->down, "%s weights: gate/up/down pointer is NULL", what);
+    MOE_CHECK(aligned(w->gate, 16) && aligned(w->up, 16) && aligned(w->down, 16),
+              "%s weights: pointers must be 16-byte aligned", what);
+    if (w->bits == 4) {
+        MOE_CHECK(w->group_size == 64, "%s weights: group_size = %d (only 64)", what, w->group_size);
+        MOE_CHECK(w->gate_scale && w->gate_bias && w->up_scale && w->up_bias && w->down_scale &&
+                      w->down_bias,
+                  "%s weights: 4-bit scale/bias pointer is NULL", what);
+        return fail(MOE_ERR_INVALID, "%s weights: the affine 4-bit path is not available in "
+                                     "this build", what);
+    }
+    return MOE_OK;
+}
+
+int check_dims(int64_t T, int32_t d, int32_t I, int32_t E, int32_t K) {
+    MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
+    MOE_CHECK(d >= 128 && d % 128 == 0, "d = %d must be a positive multiple of 128", d);
+    MOE_CHECK(I >= 128 && I % 128 == 0, "I = %d must be a positive multiple of 128", I);
+    MOE_CHECK(E >= 1 && E <= kMaxExperts, "E = %d outside [1, %d]", E, kMaxExperts);
+    MOE_CHECK(K >= 1 && K <= kMaxTopK, "K = %d outside [1, %d]", K, kMaxTopK);
+    MOE_CHECK(T * (int64_t)K + T < ((int64_t)1 << 31), "T*K = %lld too large",
+              (long long)(T * (int64_t)K));
+    return MOE_OK;
+}
+
+// Token tile of the expert GEMMs: tokens on the N side (16..64) when the experts see few
+// tokens on average, else 128-token tiles on the M side.
+int expert_tok_tile(int64_t P, int32_t E) {
+    const int64_t avg = (P + E - 1) / E;
+    if (avg <= 12) return 16;
+    if (avg <= 24) return 32;
+    if (avg <= 48) return 64;
+    return 0;
+}
+
+struct RouterPlan {
+    int tok_tile;
+    int ksplit;
+    long long tiles;
+};
+
+RouterPlan router_plan(int64_t T, int32_t d, int32_t E) {
+    RouterPlan rp;
+    const int nsm = moe::num_sms();
+    long long ttiles, ftiles;
+    if (T <= 256) {
+        rp.tok_tile = T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128;
+        ttiles = (T + rp.tok_tile - 1) / rp.tok_tile;
+        ftiles = (E + 127) / 128;
+    } else {
+        rp.tok_tile = 0;
+        ttiles = (T + 127) / 128;
+        ftiles = (E + 255) / 256;
+    }
+    const int nkb = d / 64;
+    rp.ksplit = 1;
+    for (int ks = 1; ks <= nkb; ++ks)
+        if (nkb % ks == 0 && ttiles * ftiles * ks <= nsm) rp.ksplit = ks;
+    rp.tiles = ttiles * ftiles * rp.ksplit;
+    return rp;
+}
+
+// Workspace of the expert SwiGLU: x_perm [P, d] and h [P + T, I].
+struct SwigluWs {
+    size_t x_perm, h, total;
+};
+SwigluWs swiglu_ws(int64_t T, int32_t d, int32_t I, int32_t K, int has_shared) {
+    SwigluWs w;
+    const int64_t P = T * K;
+    size_t off = 0;
+    w.x_perm = off;
+    off += align256((size_t)P * d * 2);
+    w.h = off;
+    off += align256((size_t)(P + (has_shared ? T : 0)) * I * 2);
+    w.total = off;
+    return w;
+}
+
+// Whole-layer workspace.
+struct ForwardWs {
+    size_t logits_part, inds, scores, counts, offsets, perm, inv, expert_out, swiglu, total;
+};
+ForwardWs forward_ws(int64_t T, int32_t d, int32_t I, int32_t E, int32_t K, int has_shared,
+                     int ksplit) {
+    ForwardWs w;
+    const int64_t P = T * K;
+    size_t off = 0;
+    w.logits_part = off; off += align256((size_t)ksplit * T * E * 4);
+    w.inds = off;        off += align256((size_t)P * 4);
+    w.scores = off;      off += align256((size_t)P * 4);
+    w.counts = off;      off += align256((size_t)E * 4);
+    w.offsets = off;     off += align256((size_t)(E + 1) * 4);
+    w.perm = off;        off += align256((size_t)P * 4);
+    w.inv = off;         off += align256((size_t)P * 4);
+    w.expert_out = off;  off += align256((size_t)(P + (has_shared ? T : 0)) * d * 2);
+    w.swiglu = off;      off += swiglu_ws(T, d, I, K, has_shared).total;
+    w.total = off;
+    return w;
+}
+
+// Maximum K-split of the router over every device plan (the workspace must not depend on
+// the device it is sized on): d/64 k-blocks at most.
+int router_ksplit_bound(int32_t d) { return d / 64; }
+
+int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_t K,
+               const int32_t* offsets, const int32_t* perm, const moe_expert_weights_t* ex,
+               const moe_expert_weights_t* sh, void* out, uint8_t* ws, cudaStream_t s) {
+    const int64_t P = T * K;
+    const SwigluWs lw = swiglu_ws(T, d, I, K, sh != nullptr);
+    void* x_perm = ws + lw.x_perm;
+    void* h = ws + lw.h;
+    const int has_shared = sh != nullptr;
+    MOE_CUDA(moe::launch_gather_rows(x, perm, offsets, E, K, P, d, x_perm, s), "gather rows");
+    MOE_CUDA(phase(4, s), "phase event");
+    const int tok = expert_tok_tile(P, E);
+    const int tokn = tok ? tok : 128;
+    const long long mt_bound = (P + tokn - 1) / tokn + E + (has_shared ? (T + tokn - 1) / tokn : 0);
+
+    moe::GemmArgs g = {};
+    g.mode = moe::kGateUp;
+    g.act = x_perm;
+    g.act_rows = P;
+    g.act_shared = x;
+    g.shared_act_row0 = 0;
+    g.offsets = offsets;
+    g.E = E;
+    g.has_shared = has_shared;
+    g.shared_rows = T;
+    g.shared_out_row0 = P;
+    g.Kdim = d;
+    g.F = I;
+    g.ksplit = 1;
+    g.w = {ex->bits, ex->gate, ex->up, ex->gate_scale, ex->gate_bias, ex->up_scale, ex->up_bias};
+    if (has_shared) g.ws = {16, sh->gate, sh->up, nullptr, nullptr, nullptr, nullptr};
+    g.out = h;
+    g.out_ld = I;
+    g.tok_tile = tok;
+    g.max_tiles = mt_bound * (I / 128);
+    MOE_CUDA(moe::launch_gemm(g, s), "gate/up GEMM");
+    MOE_CUDA(phase(5, s), "phase event");
+
+    moe::GemmArgs dn = g;
+    dn.mode = moe::kDown;
+    dn.act = h;
+    dn.act_rows = P + (has_shared ? T : 0);
+    dn.act_shared = h;
+    dn.shared_act_row0 = P;
+    dn.Kdim = I;
+    dn.F = d;
+    dn.w = {ex->bits, ex->down, nullptr, ex->down_scale, ex->down_bias, nullptr, nullptr};
+    if (has_shared) dn.ws = {16, sh->down, nullptr, nullptr, nullptr, nullptr, nullptr};
+    dn.out = out;
+    dn.out_ld = d;
+    dn.max_tiles = mt_bound * ((d + (tok ? 127 : 255)) / (tok ? 128 : 256));
+    MOE_CUDA(moe::launch_gemm(dn, s), "down GEMM");
+    MOE_CUDA(phase(6, s), "phase event");
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_err.c_str(); }
+
+int32_t moe_version(void) { return 100; }
+
+int moe_device_status(int32_t clear, moe_stream_t stream) {
+    int rc = check_device();
+    if (rc) return rc;
+    unsigned int st = 0;
+    MOE_CUDA(moe::read_device_status(&st, clear, (cudaStream_t)stream), "status read");
+    if (st != 0) return fail(MOE_ERR_TIMEOUT, "a device-side wait gave up (status %u)", st);
+    return MOE_OK;
+}
+
+int moe_route_deepseek(const void* logits, moe_dtype_t dtype, int64_t rows, int32_t E,
+                       const float* bias, const moe_route_params_t* params, int32_t* inds,
+                       float* scores, moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(logits && bias && inds && scores, "NULL pointer argument");
+    MOE_CHECK(dtype == MOE_DTYPE_F32 || dtype == MOE_DTYPE_BF16, "dtype %d unknown", (int)dtype);
+    MOE_CHECK(rows >= 0, "rows = %lld < 0", (long long)rows);
+    int rc = check_route_params(E, params);
+    if (rc) return rc;
+    if (rows == 0) return MOE_OK;
+    rc = check_device();
+    if (rc) return rc;
+    moe::RouteArgs a = {};
+    a.logits = logits;
+    a.bf16 = dtype == MOE_DTYPE_BF16;
+    a.nsplit = 1;
+    a.split_stride = 0;
+    a.logit_offset = nullptr;
+    a.bias = bias;
+    a.rows = rows;
+    a.E = E;
+    a.top_k = params->top_k;
+    a.n_group = params->n_group;
+    a.topk_group = params->topk_group;
+    a.norm = params->norm_topk_prob != 0;
+    a.scale = params->routed_scaling_factor;
+    a.inds = inds;
+    a.scores = scores;
+    a.logits_out = nullptr;
+    MOE_CUDA(moe::launch_route(a, (cudaStream_t)stream), "route kernel");
+    return MOE_OK;
+}
+
+int moe_permute(const int32_t* inds, int64_t T, int32_t K, int32_t E, int32_t* counts,
+                int32_t* offsets, int32_t* perm, int32_t* inv_perm, moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(inds && counts && offsets && perm && inv_perm, "NULL pointer argument");
+    MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
+    MOE_CHECK(K >= 1, "K = %d < 1", K);
+    MOE_CHECK(E >= 1 && E <= kMaxExperts, "E = %d outside [1, %d]", E, kMaxExperts);
+    MOE_CHECK(T * (int64_t)K < ((int64_t)1 << 31), "T*K too large");
+    int rc = check_device();
+    if (rc) return rc;
+    MOE_CUDA(moe::launch_permute(inds, T * K, E, counts, offsets, perm, inv_perm,
+                                 (cudaStream_t)stream),
+             "permute kernel");
+    return MOE_OK;
+}
+
+int moe_router_logits(const void* x, int64_t T, int32_t d, const void* w_router, int32_t E,
+                      const float* logit_offset, float* logits, moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(x && w_router && logits, "NULL pointer argument");
+    MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
+    MOE_CHECK(d >= 64 && d % 64 == 0, "d = %d must be a positive multiple of 64", d);
+    MOE_CHECK(E >= 1 && E <= kMaxExperts, "E = %d outside [1, %d]", E, kMaxExperts);
+    MOE_CHECK(aligned(x, 16) && aligned(w_router, 16), "x and w_router must be 16-byte aligned");
+    if (T == 0) return MOE_OK;
+    int rc = check_device();
+    if (rc) return rc;
+    // one K split, written straight to `logits`, then the offset is added by the gate's
+    // reduction kernel only when requested
+    moe::GemmArgs g = {};
+    g.mode = moe::kRouter;
+    g.act = x;
+    g.act_rows = T;
+    g.offsets = nullptr;
+    g.single_rows = T;
+    g.E = 1;
+    g.Kdim = d;
+    g.F = E;
+    g.ksplit = 1;
+    g.split_stride = 0;
+    g.w = {16, w_router, nullptr, nullptr, nullptr, nullptr, nullptr};
+    g.out = logits;
+    g.out_ld = E;
+    g.tok_tile = T <= 256 ? (T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128) : 0;
+    const int tokn = g.tok_tile ? g.tok_tile : 128;
+    g.max_tiles = ((T + tokn - 1) / tokn) * ((E + (g.tok_tile ? 127 : 255)) / (g.tok_tile ? 128 : 256));
+    MOE_CUDA(moe::launch_gemm(g, (cudaStream_t)stream), "router GEMM");
+    if (logit_offset)
+        MOE_CUDA(moe::launch_add_offset(logits, T, E, logit_offset, (cudaStream_t)stream),
+                 "logit offset");
+    return MOE_OK;
+}
+
+size_t moe_grouped_swiglu_workspace_bytes(int64_t T, int32_t d, int32_t I, int32_t E, int32_t K,
+                                          int32_t has_shared) {
+    (void)E;
+    if (T < 0 || d < 0 || I < 0 || K < 0) return 0;
+    return swiglu_ws(T, d, I, K, has_shared != 0).total;
+}
+
+int moe_grouped_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_t K,
+                       const int32_t* offsets, const int32_t* perm,
+                       const moe_expert_weights_t* experts, const moe_expert_weights_t* shared,
+                       void* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(x && offsets && perm && out && ws, "NULL pointer argument");
+    int rc = check_dims(T, d, I, E, K);
+    if (rc) return rc;
+    rc = check_weights(experts, "expert", 0);
+    if (rc) return rc;
+    if (shared) {
+        rc = check_weights(shared, "shared expert", 1);
+        if (rc) return rc;
+    }
+    MOE_CHECK(aligned(x, 16) && aligned(out, 16), "x and out must be 16-byte aligned");
+    MOE_CHECK(aligned(ws, 256), "ws must be 256-byte aligned");
+    const size_t need = swiglu_ws(T, d, I, K, shared != nullptr).total;
+    MOE_CHECK(ws_bytes >= need, "ws_bytes = %zu < %zu required", ws_bytes, need);
+    if (T == 0) return MOE_OK;
+    rc = check_device();
+    if (rc) return rc;
+    return run_swiglu(x, T, d, I, E, K, offsets, perm, experts, shared, out,
+                      static_cast<uint8_t*>(ws), (cudaStream_t)stream);
+}
+
+int moe_combine(const void* expert_out, const float* scores, const int32_t* inv_perm,
+                const void* shared_out, int64_t T, int32_t K, int32_t d, void* y,
+                moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(expert_out && scores && inv_perm && y, "NULL pointer argument");
+    MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
+    MOE_CHECK(K >= 1, "K = %d < 1", K);
+    MOE_CHECK(d >= 8 && d % 8 == 0, "d = %d must be a positive multiple of 8", d);
+    MOE_CHECK(aligned(expert_out, 16) && aligned(y, 16) && (!shared_out || aligned(shared_out, 16)),
+              "expert_out, shared_out and y must be 16-byte aligned");
+    if (T == 0) return MOE_OK;
+    int rc = check_device();
+    if (rc) return rc;
+    MOE_CUDA(moe::launch_combine(expert_out, scores, inv_perm, shared_out, T, K, d, y,
+                                 (cudaStream_t)stream),
+             "combine kernel");
+    return MOE_OK;
+}
+
+size_t moe_forward_workspace_bytes(int64_t T, int32_t d, int32_t I, int32_t E, int32_t top_k,
+                                   int32_t has_shared) {
+    if (T < 0 || d < 0 || I < 0 || E < 0 || top_k < 0) return 0;
+    return forward_ws(T, d, I, E, top_k, has_shared != 0, router_ksplit_bound(d)).total;
+}
+
+int moe_forward(const void* x, int64_t T, int32_t d, int32_t I, int32_t E,
+                const void* w_router, const float* bias, const float* logit_offset,
+                const moe_route_params_t* params, const moe_expert_weights_t* experts,
+                const moe_expert_weights_t* shared, void* y, int32_t* inds_out,
+                float* scores_out, float* logits_out, void* ws, size_t ws_bytes,
+                moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(x && w_router && bias && y && ws, "NULL pointer argument");
+    int rc = check_route_params(E, params);
+    if (rc) return rc;
+    const int32_t K = params->top_k;
+    rc = check_dims(T, d, I, E, K);
+    if (rc) return rc;
+    rc = check_weights(experts, "expert", 0);
+    if (rc) return rc;
+    if (shared) {
+        rc = check_weights(shared, "shared expert", 1);
+        if (rc) return rc;
+    }
+    MOE_CHECK(aligned(x, 16) && aligned(w_router, 16) && aligned(y, 16),
+              "x, w_router and y must be 16-byte aligned");
+    MOE_CHECK(aligned(ws, 256), "ws must be 256-byte aligned");
+    const int has_shared = shared != nullptr;
+    const ForwardWs lw = forward_ws(T, d, I, E, K, has_shared, router_ksplit_bound(d));
+    MOE_CHECK(ws_bytes >= lw.total, "ws_bytes = %zu < %zu required", ws_bytes, lw.total);
+    if (T == 0) return MOE_OK;
+    rc = check_device();
+    if (rc) return rc;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    const int64_t P = T * K;
+    float* lpart = reinterpret_cast<float*>(w + lw.logits_part);
+    int32_t* inds = inds_out ? inds_out : reinterpret_cast<int32_t*>(w + lw.inds);
+    float* scores = scores_out ? scores_out : reinterpret_cast<float*>(w + lw.scores);
+    int32_t* counts = reinterpret_cast<int32_t*>(w + lw.counts);
+    int32_t* offsets = reinterpret_cast<int32_t*>(w + lw.offsets);
+    int32_t* perm = reinterpret_cast<int32_t*>(w + lw.perm);
+    int32_t* inv = reinterpret_cast<int32_t*>(w + lw.inv);
+    void* eo = w + lw.expert_out;
+
+    MOE_CUDA(phase(0, s), "phase event");
+    // a1: router linear, K-split partial sums
+    const RouterPlan rp = router_plan(T, d, E);
+    moe::GemmArgs g = {};
+    g.mode = moe::kRouter;
+    g.act = x;
+    g.act_rows = T;
+    g.offsets = nullptr;
+    g.single_rows = T;
+    g.E = 1;
+    g.Kdim = d;
+    g.F = E;
+    g.ksplit = rp.ksplit;
+    g.split_stride = (long long)T * E;
+    g.w = {16, w_router, nullptr, nullptr, nullptr, nullptr, nullptr};
+    g.out = lpart;
+    g.out_ld = E;
+    g.tok_tile = rp.tok_tile;
+    g.max_tiles = rp.tiles;
+    MOE_CUDA(moe::launch_gemm(g, s), "router GEMM");
+    MOE_CUDA(phase(1, s), "phase event");
+
+    // a2: gate (sums the partials in split order, adds the offset)
+    moe::RouteArgs ra = {};
+    ra.logits = lpart;
+    ra.bf16 = 0;
+    ra.nsplit = rp.ksplit;
+    ra.split_stride = (long long)T * E;
+    ra.logit_offset = logit_offset;
+    ra.bias = bias;
+    ra.rows = T;
+    ra.E = E;
+    ra.top_k = K;
+    ra.n_group = params->n_group;
+    ra.topk_group = params->topk_group;
+    ra.norm = params->norm_topk_prob != 0;
+    ra.scale = params->routed_scaling_factor;
+    ra.inds = inds;
+    ra.scores = scores;
+    ra.logits_out = logits_out;
+    MOE_CUDA(moe::launch_route(ra, s), "route kernel");
+    MOE_CUDA(phase(2, s), "phase event");
+
+    // a3: dispatch
+    MOE_CUDA(moe::launch_permute(inds, P, E, counts, offsets, perm, inv, s), "permute kernel");
+    MOE_CUDA(phase(3, s), "phase event");
+
+    // a4 + a5 (+ a7): expert SwiGLU GEMMs, shared expert as the last group
+    rc = run_swiglu(x, T, d, I, E, K, offsets, perm, experts, shared, eo, w + lw.swiglu, s);
+    if (rc) return rc;
+
+    // a6: combine
+    const void* so = has_shared ? static_cast<const void*>(static_cast<const uint8_t*>(eo) +
+                                                           (size_t)P * d * 2)
+                                : nullptr;
+    MOE_CUDA(moe::launch_combine(eo, scores, inv, so, T, K, d, y, s), "combine kernel");
+    MOE_CUDA(phase(7, s), "phase event");
+    return MOE_OK;
+}
+
+int moe_set_phase_events(void* const* events, int32_t n) {
+    g_err.clear();
+    MOE_CHECK(n >= 0 && n <= kMaxPhaseEvents, "n = %d outside [0, %d]", n, kMaxPhaseEvents);
+    MOE_CHECK(n == 0 || events, "events is NULL");
+    for (int i = 0; i < n; ++i) g_phase_ev[i] = static_cast<cudaEvent_t>(events[i]);
+    g_phase_n = events ? n : 0;
+    return MOE_OK;
+}
+
+}  // extern "C"

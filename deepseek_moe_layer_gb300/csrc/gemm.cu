@@ -1,0 +1,582 @@
+// gemm.cu -- grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// fed by TMA, with a per-expert tile scheduler that runs entirely on the device.
+//
+// Source: "Epic: Engine Inference Core Stage E - MoE + hybrid families", first paragraph
+// (switch_glu over the dispatched tokens through gather_mm / gather_qmm) and
+// "feat(engine): E1 DeepSeek-style MoE gate (sigmoid, group top-k, bias) (#108)", review
+// section "Architecture and design" (switch_glu, then combine with the shared expert).
+// Three products use the same kernel:
+//   kGateUp : h[j, n] = silu(x_j . W_gate[e, n]) * (x_j . W_up[e, n])      (SwiGLU fused)
+//   kDown   : o[j, c] = h_j . W_down[e, c]
+//   kRouter : logits[t, e] = x_t . W_router[e]     (fp32 out, optional K split)
+//
+// Groups: the E routed experts (rows offsets[g] .. offsets[g+1] of the activation
+// matrix) plus, optionally, the shared expert as group E (all T tokens).  A tile is
+// (group, token tile, feature tile, k split); the tile list is derived on the device from
+// the expert offsets, so no host synchronisation sits between dispatch and GEMM.  Tiles
+// are ordered group-major, feature tile next, token tile fastest, so CTAs working at the
+// same time share a weight tile through L2.
+//
+// Two orientations:
+//   tokens on M (TOKT == 0): UMMA 128 x 256; A = 128 token rows, B = 256 weight rows
+//       (kGateUp: 128 gate rows then the same 128 up rows, so one accumulator row holds
+//       matching gate and up columns and the SwiGLU epilogue is thread-local).
+//   tokens on N (TOKT = 16..128): UMMA 128 x TOKT; A = 128 weight rows (kGateUp: two
+//       A tiles, gate and up, into two accumulators), B = TOKT token rows.  Used when the
+//       experts see few tokens (decode): the weight stream is the whole cost, and putting
+//       the tokens on N wastes no tensor work or shared-memory bandwidth on padding.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer: a ring of kStages (activation tile, weight tile) stages;
+//   warp 1      TMEM owner and UMMA issuer (one elected lane); accumulators double
+//               buffered in TMEM so the epilogue of tile i overlaps the main loop of i+1;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, SwiGLU / conversion, stores.
+// Every mbarrier wait is bounded; a role that gives up records a timeout in the device
+// status word, tells the others through shared memory, waits for its own copies and
+// MMAs in flight, and the CTA frees its TMEM and returns.
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+__device__ unsigned int g_status;
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBK = 64;  // bf16 elements per 128-byte swizzled row = one k-block
+
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+__host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ constexpr int pow2ceil(int v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+template <int MODE, int TOKT>
+struct Cfg {
+    static constexpr bool kSwap = TOKT != 0;
+    static constexpr int kTok = kSwap ? TOKT : 128;                  // tokens per tile
+    static constexpr int kNW = (kSwap && MODE == kGateUp) ? 2 : 1;   // A weight tiles (swap)
+    static constexpr int kWRows = kSwap ? 128 * kNW : 256;           // weight rows per stage
+    static constexpr int kFeat = kSwap ? 128 : (MODE == kGateUp ? 128 : 256);
+    static constexpr int kXBytes = kTok * 128;
+    static constexpr int kWBytes = kWRows * 128;
+    static constexpr int kStageBytes = kXBytes + kWBytes;
+    static constexpr int kStages = cmin(12, (200 * 1024) / kStageBytes);
+    static constexpr int kAccCols = kSwap ? kTok * kNW : 256;
+    static constexpr int kTmemCols = pow2ceil(cmax(32, 2 * kAccCols));
+    static constexpr int kN = kSwap ? kTok : 256;
+    static constexpr uint32_t kIdesc = idesc_bf16(128, kN);
+    static constexpr int kMaxGroups = 1025;
+    // shared memory: stages | barriers | misc | tile prefix | row offsets
+    static constexpr int kBarOff = kStages * kStageBytes;
+    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+    static constexpr int kPrefixOff = kMiscOff + 16;
+    static constexpr int kRowOffOff = kPrefixOff + 4 * (kMaxGroups + 1);
+    static constexpr int kSmemBytes = kRowOffOff + 4 * (kMaxGroups + 1) + 1024;  // + align
+    static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kN % 16 == 0 && kN >= 16 && kN <= 256, "UMMA N for M = 128");
+};
+
+struct KParams {
+    const int32_t* offsets;
+    long long single_rows;
+    int E;
+    int has_shared;
+    long long shared_rows;
+    long long shared_act_row0;
+    long long shared_out_row0;
+    int Kdim;
+    int F;
+    int ksplit;
+    long long split_stride;
+    void* out;
+    long long out_ld;
+};
+
+struct TileInfo {
+    int g;               // group (E = shared)
+    bool shared;
+    long long act_row;   // first activation row of the tile
+    long long out_row;   // first output row of the tile
+    int rows;            // valid token rows in the tile
+    int f;               // feature tile
+    int kb0, kb1;        // k-block range
+    int ks;              // k split
+};
+
+// Tiles of group g: ceil(rows_g / kTok) token tiles x feature tiles x k splits.
+template <class C>
+MOE_DEV int group_tiles(long long rows, int ftiles, int ksplit) {
+    return (int)((rows + C::kTok - 1) / C::kTok) * ftiles * ksplit;
+}
+
+template <class C>
+MOE_DEV long long group_rows(const KParams& p, const int32_t* rowoff, int g) {
+    if (!p.offsets) return p.single_rows;
+    if (g == p.E) return p.shared_rows;
+    return (long long)(rowoff[g + 1] - rowoff[g]);
+}
+
+template <class C>
+MOE_DEV TileInfo decode_tile(const KParams& p, const int32_t* prefix, const int32_t* rowoff,
+                             int ngroups, int t) {
+    // largest g with prefix[g] <= t (empty groups repeat the prefix and are skipped)
+    int lo = 0, hi = ngroups - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    TileInfo ti;
+    ti.g = lo;
+    ti.shared = p.offsets && lo == p.E;
+    const long long rows = group_rows<C>(p, rowoff, lo);
+    const int mt = (int)((rows + C::kTok - 1) / C::kTok);
+    const int ft = (p.F + C::kFeat - 1) / C::kFeat;
+    int local = t - prefix[lo];
+    const int m = local % mt;
+    local /= mt;
+    ti.f = local % ft;
+    ti.ks = local / ft;
+    const long long r0 = (long long)m * C::kTok;
+    ti.rows = (int)((rows - r0) < C::kTok ? (rows - r0) : C::kTok);
+    if (ti.shared) {
+        ti.act_row = p.shared_act_row0 + r0;
+        ti.out_row = p.shared_out_row0 + r0;
+    } else {
+        const long long base = p.offsets ? (long long)rowoff[lo] : 0;
+        ti.act_row = base + r0;
+        ti.out_row = base + r0;
+    }
+    const int nkb = p.Kdim / kBK / p.ksplit;
+    ti.kb0 = ti.ks * nkb;
+    ti.kb1 = ti.kb0 + nkb;
+    return ti;
+}
+
+MOE_DEV void record_timeout(volatile int* abort) {
+    *abort = 1;
+    atomicCAS(&g_status, 0u, kStatusTimeout);
+}
+
+template <int MODE, int TOKT>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
+                    const __grid_constant__ CUtensorMap tm_act_sh,
+                    const __grid_constant__ CUtensorMap tm_w0,
+                    const __grid_constant__ CUtensorMap tm_w1,
+                    const __grid_constant__ CUtensorMap tm_sw0,
+                    const __grid_constant__ CUtensorMap tm_sw1, const KParams p) {
+    using C = Cfg<MODE, TOKT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::kStages;
+    uint64_t* tfull = bars + 2 * C::kStages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* done = tfull + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+    int32_t* prefix = reinterpret_cast<int32_t*>(smem + C::kPrefixOff);
+    int32_t* rowoff = reinterpret_cast<int32_t*>(smem + C::kRowOffOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ngroups = p.offsets ? p.E + p.has_shared : 1;
+    const int ftiles = (p.F + C::kFeat - 1) / C::kFeat;
+
+    // ---- set-up: barriers, TMEM, group offsets and the tile prefix ----
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&tfull[0], 1);
+        mbar_init(&tfull[1], 1);
+        mbar_init(&tempty[0], 128);
+        mbar_init(&tempty[1], 128);
+        mbar_init(done, 1);
+        *abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_act_sh);
+        prefetch_tmap(&tm_w0);
+        prefetch_tmap(&tm_w1);
+        prefetch_tmap(&tm_sw0);
+        prefetch_tmap(&tm_sw1);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+    if (p.offsets)
+        for (int i = threadIdx.x; i <= p.E; i += kThreads) rowoff[i] = p.offsets[i];
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (ngroups + 31) / 32;
+        const int g0 = lane * per, g1 = min(ngroups, g0 + per);
+        int local = 0;
+        for (int g = g0; g < g1; ++g)
+            local += group_tiles<C>(group_rows<C>(p, rowoff, g), ftiles, p.ksplit);
+        int incl = local;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        int run = incl - local;
+        for (int g = g0; g < g1; ++g) {
+            prefix[g] = run;
+            run += group_tiles<C>(group_rows<C>(p, rowoff, g), ftiles, p.ksplit);
+        }
+        if (lane == 31) prefix[ngroups] = incl;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = prefix[ngroups];
+
+    if (warp == 0) {
+        // =============================== TMA producer ===============================
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_x = policy_evict_last();
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
+                const CUtensorMap* am = ti.shared ? &tm_act_sh : &tm_act;
+                const CUtensorMap* w0 = ti.shared ? &tm_sw0 : &tm_w0;
+                const CUtensorMap* w1 = ti.shared ? &tm_sw1 : &tm_w1;
+                const int wrow = (ti.shared || !p.offsets ? 0 : ti.g * p.F) + ti.f * C::kFeat;
+                for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
+                    uint8_t* st = smem + s * C::kStageBytes;
+                    mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                    const int kx = kb * kBK;
+                    tma_load_2d(st, am, &full[s], kx, (int)ti.act_row, pol_x);
+                    uint8_t* wst = st + C::kXBytes;
+                    if (MODE == kGateUp) {
+                        tma_load_2d(wst, w0, &full[s], kx, wrow, pol_w);
+                        tma_load_2d(wst + 128 * 128, w1, &full[s], kx, wrow, pol_w);
+                    } else {
+                        tma_load_2d(wst, w0, &full[s], kx, wrow, pol_w);
+                    }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA can exit
+                for (int n = (it > C::kStages ? it - C::kStages : 0); n < it; ++n)
+                    mbar_wait(&full[n % C::kStages], (uint32_t)(n / C::kStages) & 1u, nullptr,
+                              100000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================ UMMA issuer ===============================
+        if (lane == 0) {
+            int it = 0, lt = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
+                const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
+                const int ab = lt & 1;
+                const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+                if (!mbar_wait(&tempty[ab], aph ^ 1u, abort)) { record_timeout(abort); break; }
+                tc_fence_after();
+                const uint32_t acc = tmem_base + (uint32_t)(ab * C::kAccCols);
+                for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++it) {
+                    const int s = it % C::kStages;
+                    const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
+                    if (!mbar_wait(&full[s], ph, abort)) { record_timeout(abort); ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t xs = smem_u32(smem + s * C::kStageBytes);
+                    const uint32_t ws = xs + C::kXBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint32_t accum = (kb > ti.kb0 || kk > 0) ? 1u : 0u;
+                        if (C::kSwap) {
+                            const uint64_t bd = sdesc_k128(xs + kk * 32);
+#pragma unroll
+                            for (int w = 0; w < C::kNW; ++w)
+                                umma_bf16(acc + (uint32_t)(w * C::kTok),
+                                          sdesc_k128(ws + w * 128 * 128 + kk * 32), bd,
+                                          C::kIdesc, accum);
+                        } else {
+                            umma_bf16(acc, sdesc_k128(xs + kk * 32), sdesc_k128(ws + kk * 32),
+                                      C::kIdesc, accum);
+                        }
+                    }
+                    umma_commit(&empty[s]);
+                }
+                if (!ok) break;
+                umma_commit(&tfull[ab]);
+            }
+            // drain every UMMA issued by this thread before TMEM can be released
+            if (it > 0) {
+                umma_commit(done);
+                mbar_wait(done, 0u, nullptr, 100000000ull);
+            }
+        }
+    } else {
+        // ================================= epilogue =================================
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int lt = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+            const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
+            const int ab = lt & 1;
+            const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+            if (!mbar_wait(&tfull[ab], aph, abort)) { record_timeout(abort); break; }
+            tc_fence_after();
+            const uint32_t tacc =
+                tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kAccCols);
+            if (!C::kSwap) {
+                // accumulator row = token row (q*32 + lane), columns = features
+                const int r = q * 32 + lane;
+                const bool valid = r < ti.rows;
+                const long long orow = ti.out_row + r;
+                if (MODE == kGateUp) {
+                    __nv_bfloat16_raw* dst = static_cast<__nv_bfloat16_raw*>(p.out) +
+                                             orow * p.out_ld + (long long)ti.f * 128;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 128; c0 += 32) {
+                        uint32_t g[32], u[32];
+                        __syncwarp();
+                        tmem_ld32(tacc + c0, g);
+                        tmem_ld32(tacc + 128 + c0, u);
+                        tmem_ld_wait();
+                        if (valid) {
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                uint32_t w4[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int c = v * 8 + i * 2;
+                                    w4[i] = pack_bf16x2(
+                                        silu(__uint_as_float(g[c])) * __uint_as_float(u[c]),
+                                        silu(__uint_as_float(g[c + 1])) * __uint_as_float(u[c + 1]));
+                                }
+                                d4[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                            }
+                        }
+                    }
+                } else {
+                    const int fbase = ti.f * 256;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 256; c0 += 32) {
+                        uint32_t a[32];
+                        __syncwarp();
+                        tmem_ld32(tacc + c0, a);
+                        tmem_ld_wait();
+                        if (valid && fbase + c0 < p.F) {
+                        if (MODE == kDown) {
+                            __nv_bfloat16_raw* dst = static_cast<__nv_bfloat16_raw*>(p.out) +
+                                                     orow * p.out_ld + fbase + c0;
+                            if (fbase + c0 + 32 <= p.F) {
+                                uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                                for (int v = 0; v < 4; ++v)
+                                    d4[v] = make_uint4(
+                                        pack_bf16x2(__uint_as_float(a[v * 8 + 0]), __uint_as_float(a[v * 8 + 1])),
+                                        pack_bf16x2(__uint_as_float(a[v * 8 + 2]), __uint_as_float(a[v * 8 + 3])),
+                                        pack_bf16x2(__uint_as_float(a[v * 8 + 4]), __uint_as_float(a[v * 8 + 5])),
+                                        pack_bf16x2(__uint_as_float(a[v * 8 + 6]), __uint_as_float(a[v * 8 + 7])));
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    if (fbase + c0 + i < p.F)
+                                        dst[i].x = (unsigned short)(pack_bf16x2(__uint_as_float(a[i]), 0.0f) & 0xFFFFu);
+                            }
+                        } else {
+                            float* dst = static_cast<float*>(p.out) + (long long)ti.ks * p.split_stride +
+                                         orow * p.out_ld + fbase + c0;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (fbase + c0 + i < p.F) dst[i] = __uint_as_float(a[i]);
+                        }
+                        }
+                    }
+                }
+            } else {
+                // accumulator row = feature (q*32 + lane), columns = tokens
+                const int feat = ti.f * 128 + q * 32 + lane;
+                const bool fvalid = feat < p.F;
+#pragma unroll 1
+                for (int j0 = 0; j0 < C::kTok; j0 += 16) {
+                    uint32_t a[16], b[16];
+                    __syncwarp();
+                    tmem_ld16(tacc + j0, a);
+                    if (MODE == kGateUp) tmem_ld16(tacc + C::kTok + j0, b);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = j0 + jj;
+                        if (!fvalid || j >= ti.rows) break;
+                        const long long orow = ti.out_row + j;
+                        if (MODE == kGateUp) {
+                            const float h = silu(__uint_as_float(a[jj])) * __uint_as_float(b[jj]);
+                            static_cast<__nv_bfloat16_raw*>(p.out)[orow * p.out_ld + feat].x =
+                                (unsigned short)(pack_bf16x2(h, 0.0f) & 0xFFFFu);
+                        } else if (MODE == kDown) {
+                            static_cast<__nv_bfloat16_raw*>(p.out)[orow * p.out_ld + feat].x =
+                                (unsigned short)(pack_bf16x2(__uint_as_float(a[jj]), 0.0f) & 0xFFFFu);
+                        } else {
+                            static_cast<float*>(p.out)[(long long)ti.ks * p.split_stride +
+                                                       orow * p.out_ld + feat] = __uint_as_float(a[jj]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[ab]);
+        }
+    }
+
+    // ---- tear-down ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous), box of 64 columns x box_rows rows,
+// 128-byte swizzle, out-of-range elements read as zero.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    if (rows < 1) rows = 1;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE, int TOKT>
+cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
+    using C = Cfg<MODE, TOKT>;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, TOKT>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    const int wbox = C::kSwap ? 128 : (MODE == kGateUp ? 128 : 256);
+    const long long wrows_routed = (long long)(a.offsets ? a.E : 1) * a.F;
+    CUtensorMap m_act, m_act_sh, m_w0, m_w1, m_sw0, m_sw1;
+    bool ok = make_map(&m_act, a.act, a.act_rows, a.Kdim, C::kTok);
+    ok = ok && make_map(&m_act_sh, a.act_shared ? a.act_shared : a.act,
+                        a.act_shared ? (a.shared_act_row0 + a.shared_rows) : a.act_rows, a.Kdim,
+                        C::kTok);
+    ok = ok && make_map(&m_w0, a.w.w0, wrows_routed, a.Kdim, wbox);
+    ok = ok && make_map(&m_w1, a.w.w1 ? a.w.w1 : a.w.w0, wrows_routed, a.Kdim, wbox);
+    const void* sw0 = a.has_shared ? a.ws.w0 : a.w.w0;
+    const void* sw1 = a.has_shared ? (a.ws.w1 ? a.ws.w1 : a.ws.w0) : a.w.w0;
+    const long long srows = a.has_shared ? a.F : wrows_routed;
+    ok = ok && make_map(&m_sw0, sw0, srows, a.Kdim, wbox);
+    ok = ok && make_map(&m_sw1, sw1, srows, a.Kdim, wbox);
+    if (!ok) return cudaErrorInvalidValue;
+
+    KParams p;
+    p.offsets = a.offsets;
+    p.single_rows = a.single_rows;
+    p.E = a.E;
+    p.has_shared = a.has_shared;
+    p.shared_rows = a.shared_rows;
+    p.shared_act_row0 = a.shared_act_row0;
+    p.shared_out_row0 = a.shared_out_row0;
+    p.Kdim = a.Kdim;
+    p.F = a.F;
+    p.ksplit = a.ksplit;
+    p.split_stride = a.split_stride;
+    p.out = a.out;
+    p.out_ld = a.out_ld;
+
+    long long grid = num_sms();
+    if (a.max_tiles < grid) grid = a.max_tiles;
+    if (grid < 1) return cudaSuccess;
+    moe_gemm_kernel<MODE, TOKT><<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(
+        m_act, m_act_sh, m_w0, m_w1, m_sw0, m_sw1, p);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t dispatch_tok(const GemmArgs& a, cudaStream_t s) {
+    switch (a.tok_tile) {
+        case 0: return run_gemm<MODE, 0>(a, s);
+        case 16: return run_gemm<MODE, 16>(a, s);
+        case 32: return run_gemm<MODE, 32>(a, s);
+        case 64: return run_gemm<MODE, 64>(a, s);
+        case 128: return run_gemm<MODE, 128>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
+    if (a.w.bits != 16) return cudaErrorInvalidValue;
+    switch (a.mode) {
+        case kGateUp: return dispatch_tok<kGateUp>(a, s);
+        case kDown: return dispatch_tok<kDown>(a, s);
+        case kRouter: return dispatch_tok<kRouter>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t read_device_status(unsigned int* out, int clear, cudaStream_t s) {
+    cudaError_t err = cudaMemcpyFromSymbolAsync(out, g_status, sizeof(unsigned int), 0,
+                                                cudaMemcpyDeviceToHost, s);
+    if (err != cudaSuccess) return err;
+    err = cudaStreamSynchronize(s);
+    if (err != cudaSuccess || !clear) return err;
+    const unsigned int zero = 0;
+    err = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(unsigned int), 0,
+                                  cudaMemcpyHostToDevice, s);
+    if (err != cudaSuccess) return err;
+    return cudaStreamSynchronize(s);
+}
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+    return n > 0 ? n : 1;
+}
+
+}  // namespace moe

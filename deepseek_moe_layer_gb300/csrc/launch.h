@@ -1,0 +1,87 @@
+// launch.h -- host-side launchers of the kernels (internal to the library; the public
+// interface is include/moe_gb300.h).  Every launcher assumes its arguments were checked by
+// the C-ABI layer and returns the cudaError_t of the launch.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---- gate ---------------------------------------------------------------------------
+struct RouteArgs {
+    const void* logits;          // [nsplit][rows][E], fp32 (or bf16 when bf16 != 0)
+    int bf16;
+    int nsplit;                  // partial sums to add, in split order (>= 1)
+    long long split_stride;      // elements between splits
+    const float* logit_offset;   // [E] or nullptr
+    const float* bias;           // [E]
+    long long rows;
+    int E, top_k, n_group, topk_group, norm;
+    float scale;
+    int32_t* inds;               // [rows, K]
+    float* scores;               // [rows, K]
+    float* logits_out;           // [rows, E] copy of the summed logits, or nullptr
+};
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+// logits[t, e] += offset[e] for a [T, E] fp32 matrix.
+cudaError_t launch_add_offset(float* logits, long long T, int E, const float* offset,
+                              cudaStream_t s);
+
+// ---- dispatch -----------------------------------------------------------------------
+cudaError_t launch_permute(const int32_t* inds, long long P, int E, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv, cudaStream_t s);
+// x_perm[j] = x[perm[j] / K] for the dispatched slots j < offsets[E].
+cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t* offsets, int E,
+                               int K, long long P, int d, void* x_perm, cudaStream_t s);
+
+// ---- combine ------------------------------------------------------------------------
+cudaError_t launch_combine(const void* expert_out, const float* scores, const int32_t* inv,
+                           const void* shared_out, long long T, int K, int d, void* y,
+                           cudaStream_t s);
+
+// ---- expert GEMMs (tcgen05) ---------------------------------------------------------
+enum GemmMode { kGateUp = 0, kDown = 1, kRouter = 2 };
+
+struct GemmWeights {             // one stacked weight tensor set (bf16 or affine 4-bit)
+    int bits;
+    const void* w0;              // gate (kGateUp) / down (kDown) / router (kRouter)
+    const void* w1;              // up (kGateUp only)
+    const void* s0; const void* b0;   // 4-bit scale / bias of w0
+    const void* s1; const void* b1;   // 4-bit scale / bias of w1
+};
+
+struct GemmArgs {
+    GemmMode mode;
+    const void* act;             // activation rows (bf16 [rows_total, Kdim])
+    long long act_rows;          // rows of `act`
+    const void* act_shared;      // rows of the shared group (bf16 [T, Kdim]); may alias act
+    long long shared_act_row0;   // first row of the shared group in act_shared
+    const int32_t* offsets;      // [E+1] routed group row offsets (device) or nullptr: one
+                                 // group of rows [0, single_rows)
+    long long single_rows;
+    int E;                       // routed groups
+    int has_shared;
+    long long shared_rows;       // T
+    long long shared_out_row0;   // first output row of the shared group
+    int Kdim;                    // reduction length
+    int F;                       // output features per group
+    int ksplit;                  // kRouter only: K-splits, partial sums to out + ks*split_stride
+    long long split_stride;
+    GemmWeights w;               // routed (or router) weights
+    GemmWeights ws;              // shared expert weights (bf16)
+    void* out;                   // bf16 [rows, F] (kGateUp: h, kDown: o) or fp32 (kRouter)
+    long long out_ld;
+    int tok_tile;                // 0: tokens on the M side (128-row tiles); else tokens on
+                                 // the N side in tiles of tok_tile (16/32/64/128)
+    long long max_tiles;         // host upper bound on the number of tiles
+};
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
+
+// Per-device status word of the kernels with bounded waits.
+cudaError_t read_device_status(unsigned int* out, int clear, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,155 @@
+// permute.cu -- token-to-expert dispatch: expert histogram, exclusive scan, stable
+// permutation and its inverse, and the gather of the dispatched token rows.
+//
+// Source: "Epic: Engine Inference Core Stage E - MoE + hybrid families", first paragraph:
+// the MoE forward dispatches tokens to experts for gather_mm / gather_qmm.  The grouping
+// those calls consume is made explicit here: slot j of expert e holds pair p = t*K + k,
+// slots sorted by (expert, p).
+//
+// One CTA of 32 warps.  Warp w owns the contiguous chunk w of the P pairs.  Pass 1 builds
+// a per-warp histogram in shared memory, pass 2 turns (expert, warp) counts into slot
+// bases (experts in order, warps in order inside an expert), pass 3 replays each chunk in
+// pair order, ranking equal experts inside a 32-pair step with __match_any_sync.  Chunks
+// are ordered and each step is in pair order, so the permutation is stable and
+// deterministic without any global atomics.
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int kPermWarps = 32;
+
+__global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict__ inds,
+                                                       long long P, int E,
+                                                       int32_t* __restrict__ counts,
+                                                       int32_t* __restrict__ offsets,
+                                                       int32_t* __restrict__ perm,
+                                                       int32_t* __restrict__ inv) {
+    extern __shared__ int32_t sh[];
+    int32_t* hist = sh;                      // [kPermWarps][E]
+    int32_t* wsum = sh + kPermWarps * E;     // [32] scan carries
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+
+    const long long chunk = (P + kPermWarps - 1) / kPermWarps;
+    const long long c0 = min(P, (long long)warp * chunk);
+    const long long c1 = min(P, c0 + chunk);
+    int32_t* my = hist + warp * E;
+
+    // pass 1: per-warp histogram
+    for (long long p = c0 + lane; p < c1; p += 32) {
+        const int e = inds[p];
+        if (e >= 0 && e < E) atomicAdd(&my[e], 1);
+    }
+    __syncthreads();
+
+    // pass 2: counts, exclusive scan over experts, per-(warp, expert) bases
+    const int per = (E + blockDim.x - 1) / blockDim.x;  // experts per thread (1 for E <= 1024)
+    int local = 0;
+    for (int q = 0; q < per; ++q) {
+        const int e = threadIdx.x * per + q;
+        if (e < E) {
+            int c = 0;
+            for (int w = 0; w < kPermWarps; ++w) c += hist[w * E + e];
+            counts[e] = c;
+            local += c;
+        }
+    }
+    int incl = local;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = wsum[lane];
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xFFFFFFFFu, v, off);
+            if (lane >= off) v += u;
+        }
+        wsum[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    int run = (warp > 0 ? wsum[warp - 1] : 0) + incl - local;
+    for (int q = 0; q < per; ++q) {
+        const int e = threadIdx.x * per + q;
+        if (e < E) {
+            offsets[e] = run;
+            for (int w = 0; w < kPermWarps; ++w) {
+                const int h = hist[w * E + e];
+                hist[w * E + e] = run;
+                run += h;
+            }
+        }
+    }
+    if (threadIdx.x == blockDim.x - 1) offsets[E] = wsum[31];
+    __syncthreads();
+
+    // pass 3: stable placement
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (long long base = c0; base < c1; base += 32) {
+        const long long p = base + lane;
+        const bool active = p < c1;
+        const int e = active ? inds[p] : -1;
+        const bool valid = active && e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1 - lane);
+        int pos = 0;
+        if (valid) pos = my[e] + __popc(peers & lt_mask);
+        __syncwarp();
+        if (valid && (__ffs(peers) - 1) == lane) my[e] += __popc(peers);
+        __syncwarp();
+        if (valid) {
+            perm[pos] = (int32_t)p;
+            inv[p] = pos;
+        } else if (active) {
+            inv[p] = -1;
+        }
+    }
+}
+
+// One warp per dispatched slot: x_perm[j] = x[perm[j] / K], 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
+                                                          const int32_t* __restrict__ perm,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int E, int K, long long P, int vec_per_row,
+                                                          uint4* __restrict__ x_perm) {
+    const long long j = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (j >= P || j >= offsets[E]) return;
+    const long long t = perm[j] / K;
+    const uint4* src = x + t * vec_per_row;
+    uint4* dst = x_perm + j * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const int32_t* inds, long long P, int E, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv, cudaStream_t s) {
+    const size_t smem = sizeof(int32_t) * ((size_t)kPermWarps * E + 32);
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t err = cudaFuncSetAttribute(permute_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(sizeof(int32_t) * (kPermWarps * 1024 + 32)));
+        if (err != cudaSuccess) return err;
+        attr_done = true;
+    }
+    permute_kernel<<<1, 1024, smem, s>>>(inds, P, E, counts, offsets, perm, inv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t* offsets, int E,
+                               int K, long long P, int d, void* x_perm, cudaStream_t s) {
+    if (P == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)((P + 7) / 8);
+    gather_rows_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(x), perm, offsets, E, K, P,
+                                            d / 8, static_cast<uint4*>(x_perm));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,208 @@
+/*
+ * moe_gb300.h -- C ABI of the DeepSeek-style MoE FFN forward on one GB300 (sm_103a).
+ *
+ * The layer: router linear -> sigmoid group-top-k gate with e_score_correction_bias ->
+ * token-to-expert dispatch -> expert SwiGLU GEMMs over the gathered tokens -> weighted
+ * combine plus the always-active shared expert.  Sources (page title, section):
+ *   [gate]  "feat(engine): E1 DeepSeek-style MoE gate (sigmoid, group top-k, bias) (#108)",
+ *           sections "API", "Algorithm (mlx-lm group_expert_select)", "Scope decisions",
+ *           and the review sections "What looks solid", "Findings" and "Architecture and
+ *           design";
+ *   [epic]  "Epic: Engine Inference Core Stage E - MoE + hybrid families", first paragraph
+ *           (expert dispatch through gather_mm / gather_qmm) and "Decision 5" (4-bit target
+ *           checkpoint).
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer on the current CUDA device, unless the
+ *     argument says otherwise; the caller owns all memory (outputs and workspaces too).
+ *     Row-major layouts throughout; bf16 is IEEE bfloat16, fp16 is IEEE binary16.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default stream) and
+ *     never synchronises the host, except moe_device_status().
+ *   - Return value: MOE_OK (0) or a negative code.  All argument checks run on the host
+ *     BEFORE the first launch, so on MOE_ERR_INVALID no output has been touched (the
+ *     gate's contract: outputs unchanged on failure).  MOE_ERR_CUDA means a launch failed;
+ *     outputs are then undefined.  moe_last_error() returns a thread-local message naming
+ *     the failed check.
+ *   - Device-side waits are bounded: a kernel whose wait exceeds its limit stops, leaves
+ *     its outputs undefined and records MOE_ERR_TIMEOUT in a per-device status word read
+ *     by moe_device_status().
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID = -1, /* an argument check failed; nothing was launched            */
+    MOE_ERR_CUDA = -2,    /* a CUDA call or launch failed                               */
+    MOE_ERR_TIMEOUT = -3, /* a device-side wait gave up (reported by moe_device_status) */
+    MOE_ERR_NODEVICE = -4 /* no usable sm_103 device is current                         */
+};
+
+typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype_t;
+
+/* Gate parameters ([gate] "API": the params struct of the DeepSeek route). */
+typedef struct {
+    int32_t top_k;                 /* K experts per token, 1 <= K <= min(E, 32)            */
+    int32_t n_group;               /* G >= 1, E % G == 0, E/G >= 2 when G > 1, G <= 32      */
+    int32_t topk_group;            /* 1 <= topk_group <= G                                  */
+    int32_t norm_topk_prob;        /* renormalise the K weights (only when K > 1)           */
+    float routed_scaling_factor;   /* multiplies the K weights last                         */
+} moe_route_params_t;
+
+/*
+ * Expert weights, stacked on a leading expert axis of length NE (NE = E for the routed
+ * experts, NE = 1 for the shared expert).
+ *   bits == 16: gate, up: bf16 [NE, I, d]; down: bf16 [NE, d, I]; the scale/bias
+ *               pointers are ignored.
+ *   bits == 4 : affine 4-bit, group_size 64 along the input dimension.  gate, up: uint32
+ *               [NE, I, d/8]; down: uint32 [NE, d, I/8]; element j of a row is nibble
+ *               j%8 (bits 4*(j%8)..+3, low nibble first) of word j/8; *_scale, *_bias:
+ *               fp16 [NE, I, d/64] (gate, up) and [NE, d, I/64] (down);
+ *               w = scale * q + bias.  All pointers 16-byte aligned.
+ */
+typedef struct {
+    int32_t bits;
+    int32_t group_size;
+    const void* gate;
+    const void* up;
+    const void* down;
+    const void* gate_scale;
+    const void* gate_bias;
+    const void* up_scale;
+    const void* up_bias;
+    const void* down_scale;
+    const void* down_bias;
+} moe_expert_weights_t;
+
+/* Thread-local text of the last failed check or CUDA error ("" if none). */
+const char* moe_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t moe_version(void);
+
+/* Reads (and, if clear != 0, resets) the current device's status word: MOE_OK or
+ * MOE_ERR_TIMEOUT.  Synchronises `stream` first. */
+int moe_device_status(int32_t clear, moe_stream_t stream);
+
+/*
+ * moe_route_deepseek -- the DeepSeek gate ([gate] "API" and "Algorithm").
+ *   logits [rows, E] (fp32 or bf16; any leading dims flattened to rows), bias [E] fp32
+ *   (required; pass zeros when the checkpoint has none).
+ *   Out: inds [rows, K] int32, scores [rows, K] fp32.
+ * Per row: s = sigmoid(f32(logit)); selection runs on s + bias; for G > 1 the group score
+ * is the sum of the group's two largest biased scores, and the experts of the
+ * G - topk_group worst groups are set to 0.0 (skipped when that difference is 0); the K
+ * largest biased scores are selected, in descending order with ties to the lower expert
+ * index (lower group index for group ties); the weights are the pre-bias s of the
+ * selected experts, divided by their sum only when K > 1 and norm_topk_prob (no zero-sum
+ * guard), then multiplied by routed_scaling_factor.
+ * Errors: MOE_ERR_INVALID for a NULL pointer, rows < 0, E < 1 or E > 1024, and every
+ * parameter rule listed at moe_route_params_t.  rows == 0 is a no-op.
+ */
+int moe_route_deepseek(const void* logits, moe_dtype_t dtype, int64_t rows, int32_t E,
+                       const float* bias, const moe_route_params_t* params, int32_t* inds,
+                       float* scores, moe_stream_t stream);
+
+/*
+ * moe_permute -- token-to-expert dispatch ([epic] first paragraph: the grouping that
+ * gather_mm / gather_qmm consume).  inds [T, K] int32 expert ids of the P = T*K pairs
+ * p = t*K + k.
+ * Out: counts [E] (pairs per expert), offsets [E+1] (exclusive scan, offsets[E] = number
+ * of dispatched pairs), perm [P] (slot j -> pair id, sorted by (expert, p): stable),
+ * inv_perm [P] (pair id -> slot).  A pair whose expert id is outside [0, E) is not
+ * dispatched: its inv_perm entry is -1 and offsets[E] < P.
+ * Errors: MOE_ERR_INVALID for NULL pointers, T < 0, K < 1, E < 1, E > 1024, T*K >= 2^31.
+ */
+int moe_permute(const int32_t* inds, int64_t T, int32_t K, int32_t E, int32_t* counts,
+                int32_t* offsets, int32_t* perm, int32_t* inv_perm, moe_stream_t stream);
+
+/*
+ * moe_router_logits -- the router linear (the DeepSeek body's first call, [gate]
+ * "Merge recommendation": linear(router) -> route -> switch_glu -> combine).
+ *   x bf16 [T, d], w_router bf16 [E, d], logit_offset fp32 [E] or NULL (an additive
+ *   per-expert term, the router linear's bias).  Out: logits fp32 [T, E] = x w_router^T
+ *   (+ logit_offset), bf16 products accumulated in fp32.
+ * Errors: MOE_ERR_INVALID for NULL pointers, T < 0, d % 64 != 0, E < 1, E > 1024.
+ */
+int moe_router_logits(const void* x, int64_t T, int32_t d, const void* w_router, int32_t E,
+                      const float* logit_offset, float* logits, moe_stream_t stream);
+
+/*
+ * moe_grouped_swiglu -- expert SwiGLU over the dispatched tokens (switch_glu with
+ * gather_mm / gather_qmm, [epic] first paragraph and [gate] "Architecture and design").
+ * For each slot j of expert e (token t = perm[j] / K):
+ *     out[j] = W_down[e] (silu(W_gate[e] x[t]) * (W_up[e] x[t])),  silu(a) = a/(1+e^-a),
+ * with fp32 accumulation, h rounded to bf16 between the two GEMMs, out stored as bf16.
+ * If shared != NULL the shared expert runs on every token in the same launches and its
+ * rows follow: out[P + t] = FFN_shared(x[t]).
+ *   x bf16 [T, d]; offsets [E+1] and perm [P] as produced by moe_permute; experts with
+ *   NE = E; shared (NE = 1, bits 16) or NULL.  Out: out bf16 [P (+T), d].
+ *   ws: device workspace of at least moe_grouped_swiglu_workspace_bytes() bytes,
+ *   256-byte aligned; its contents need no initialisation and are clobbered.
+ * Errors: MOE_ERR_INVALID for NULL pointers, T < 0, K < 1, E < 1 or > 1024, d or I not a
+ * multiple of 128, T*K >= 2^31, bits not 16 or 4, group_size != 64 for bits 4, shared
+ * bits != 16, misaligned pointers, or a workspace that is too small.
+ */
+int moe_grouped_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_t K,
+                       const int32_t* offsets, const int32_t* perm,
+                       const moe_expert_weights_t* experts, const moe_expert_weights_t* shared,
+                       void* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+size_t moe_grouped_swiglu_workspace_bytes(int64_t T, int32_t d, int32_t I, int32_t E,
+                                          int32_t K, int32_t has_shared);
+
+/*
+ * moe_combine -- weighted combine plus the shared expert ([gate] "Architecture and
+ * design": combine with an always-active, ungated shared expert):
+ *     y[t] = sum_k scores[t,k] * expert_out[inv_perm[t*K+k]] (+ shared_out[t]),
+ * summed in fp32 in k order, stored as bf16.  Pairs with inv_perm == -1 contribute 0.
+ *   expert_out bf16 [P, d] (slot order), scores fp32 [T, K], inv_perm [P],
+ *   shared_out bf16 [T, d] or NULL.  Out: y bf16 [T, d].
+ * Errors: MOE_ERR_INVALID for NULL pointers, T < 0, K < 1, d % 8 != 0.
+ */
+int moe_combine(const void* expert_out, const float* scores, const int32_t* inv_perm,
+                const void* shared_out, int64_t T, int32_t K, int32_t d, void* y,
+                moe_stream_t stream);
+
+/*
+ * moe_forward -- the whole layer: router linear, gate, dispatch, expert SwiGLU (+ shared
+ * expert), combine.  Arguments as in the calls above; y bf16 [T, d].  inds_out [T, K],
+ * scores_out [T, K] and logits_out [T, E] are optional copies of the intermediate results
+ * (NULL to skip).  ws: at least moe_forward_workspace_bytes() bytes, 256-byte aligned.
+ * Errors: the union of the checks of the calls above.
+ */
+int moe_forward(const void* x, int64_t T, int32_t d, int32_t I, int32_t E,
+                const void* w_router, const float* bias, const float* logit_offset,
+                const moe_route_params_t* params, const moe_expert_weights_t* experts,
+                const moe_expert_weights_t* shared, void* y, int32_t* inds_out,
+                float* scores_out, float* logits_out, void* ws, size_t ws_bytes,
+                moe_stream_t stream);
+
+size_t moe_forward_workspace_bytes(int64_t T, int32_t d, int32_t I, int32_t E, int32_t top_k,
+                                   int32_t has_shared);
+
+/*
+ * moe_set_phase_events -- a timing aid with no counterpart in the pages: while set,
+ * moe_forward records events[i] on its stream at the boundaries of its steps:
+ *   0 start, 1 after the router linear, 2 after the gate, 3 after the dispatch,
+ *   4 after the token gather, 5 after the gate/up GEMM, 6 after the down GEMM,
+ *   7 after the combine.
+ * events: n (<= 8) cudaEvent_t handles owned by the caller, or NULL / n == 0 to stop.
+ * Process-wide setting, not thread-safe; events of index >= n are not recorded.
+ * Errors: MOE_ERR_INVALID for n < 0, n > 8, or events == NULL with n > 0.
+ */
+int moe_set_phase_events(void* const* events, int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

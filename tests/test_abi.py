@@ -1,0 +1,141 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any CUDA call (the gate's
+validation matrix: "feat(engine): E1 DeepSeek-style MoE gate (sigmoid, group top-k, bias)
+(#108)", review findings L1/L2 and the author's reply)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from deepseek_moe_layer_gb300 import binding
+from deepseek_moe_layer_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "moe_gb300.h")
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails its host checks
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_matches_binding_exports():
+    assert _declared() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    so = B.build()
+    out = subprocess.run(["nm", "-D", "--defined-only", so], capture_output=True, text=True,
+                         check=True).stdout
+    syms = {l.split()[-1] for l in out.splitlines() if l.strip()}
+    for name in _declared():
+        assert name in syms, name
+    L = binding.lib()
+    for name in _declared():
+        assert hasattr(L, name)
+    assert L.moe_version() >= 100
+
+
+def _route(E=8, top_k=2, n_group=1, topk_group=1, logits=FAKE, bias=FAKE, rows=4, dtype=0):
+    p = binding.route_params(top_k, n_group, topk_group, True, 1.0)
+    L = binding.lib()
+    rc = L.moe_route_deepseek(logits, dtype, rows, E, bias, ctypes.byref(p), FAKE, FAKE, None)
+    return rc, L.moe_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(logits=None), "NULL"),
+    (dict(bias=None), "NULL"),
+    (dict(top_k=0), "top_k = 0 < 1"),
+    (dict(top_k=9), "top_k = 9 > E"),
+    (dict(E=64, top_k=33), "top_k = 33 > 32"),
+    (dict(n_group=3), "not divisible"),
+    (dict(n_group=2, topk_group=0), "topk_group"),
+    (dict(n_group=2, topk_group=3), "topk_group"),
+    (dict(n_group=1, topk_group=2), "topk_group"),
+    (dict(n_group=8, topk_group=1), "expert(s) per group"),
+    (dict(n_group=0), "n_group = 0"),
+    (dict(E=0, top_k=1), "E = 0"),
+    (dict(E=2048, top_k=2), "E = 2048"),
+    (dict(rows=-1), "rows"),
+    (dict(dtype=7), "dtype"),
+])
+def test_route_validation_matrix(kw, msg):
+    rc, err = _route(**kw)
+    assert rc == binding.MOE_ERR_INVALID
+    assert msg in err
+
+
+def test_valid_route_without_gpu_fails_loudly():
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc, err = _route()
+    assert rc == binding.MOE_ERR_NODEVICE and err
+
+
+def test_empty_route_is_noop():
+    rc, _ = _route(rows=0)
+    assert rc == binding.MOE_OK
+
+
+def _forward(T=4, d=256, I=128, E=16, bits=16, group=64, ws_bytes=None, shared=True, **pk):
+    L = binding.lib()
+    p = binding.route_params(pk.get("top_k", 4), pk.get("n_group", 4), pk.get("topk_group", 2),
+                             True, 2.5)
+    ew = binding.ExpertWeights(bits, group, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000,
+                               0x1000, 0x1000, 0x1000)
+    sw = binding.ExpertWeights(16, 0, 0x1000, 0x1000, 0x1000, None, None, None, None, None, None)
+    need = L.moe_forward_workspace_bytes(T, d, I, E, p.top_k, 1)
+    rc = L.moe_forward(FAKE, T, d, I, E, FAKE, FAKE, None, ctypes.byref(p), ctypes.byref(ew),
+                       ctypes.byref(sw) if shared else None, FAKE, None, None, None,
+                       ctypes.c_void_p(0x10000), need if ws_bytes is None else ws_bytes, None)
+    return rc, L.moe_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(d=200), "d = 200"),
+    (dict(I=100), "I = 100"),
+    (dict(T=-1), "T = -1"),
+    (dict(bits=8), "bits = 8"),
+    (dict(bits=4, group=32), "group_size = 32"),
+    (dict(ws_bytes=1024), "ws_bytes"),
+    (dict(top_k=0), "top_k"),
+    (dict(n_group=16, topk_group=1), "expert(s) per group"),
+])
+def test_forward_validation_matrix(kw, msg):
+    rc, err = _forward(**kw)
+    assert rc == binding.MOE_ERR_INVALID
+    assert msg in err
+
+
+def test_workspace_grows_with_tokens():
+    L = binding.lib()
+    a = L.moe_forward_workspace_bytes(128, 7168, 2048, 256, 8, 1)
+    b = L.moe_forward_workspace_bytes(8192, 7168, 2048, 256, 8, 1)
+    assert 0 < a < b
+    assert b % 256 == 0
+    # x_perm [P, d] + h [P+T, I] + expert_out [P+T, d] in bf16 at least
+    P, T = 8192 * 8, 8192
+    assert b >= 2 * (P * 7168 + (P + T) * 2048 + (P + T) * 7168)
+
+
+def test_permute_and_combine_validation():
+    L = binding.lib()
+    assert L.moe_permute(None, 4, 2, 8, FAKE, FAKE, FAKE, FAKE, None) == binding.MOE_ERR_INVALID
+    assert L.moe_permute(FAKE, 4, 0, 8, FAKE, FAKE, FAKE, FAKE, None) == binding.MOE_ERR_INVALID
+    assert L.moe_permute(FAKE, 4, 2, 0, FAKE, FAKE, FAKE, FAKE, None) == binding.MOE_ERR_INVALID
+    assert L.moe_combine(FAKE, FAKE, FAKE, None, 4, 2, 12, FAKE, None) == binding.MOE_ERR_INVALID
+    assert L.moe_combine(None, FAKE, FAKE, None, 4, 2, 16, FAKE, None) == binding.MOE_ERR_INVALID
+    assert L.moe_router_logits(FAKE, 4, 100, FAKE, 8, None, FAKE, None) == binding.MOE_ERR_INVALID
+
+
+def test_binding_rejects_bad_bias_rank():
+    lg = torch.zeros(2, 8)
+    with pytest.raises(ValueError):
+        binding.route_deepseek(lg, torch.zeros(1, 8), 2, 1, 1, True, 1.0)
+    with pytest.raises(ValueError):
+        binding.route_deepseek(lg, torch.zeros(7), 2, 1, 1, True, 1.0)

@@ -1,0 +1,170 @@
+"""GPU parity of the whole layer (moe_forward) and of its parts (moe_router_logits,
+moe_grouped_swiglu, moe_combine) against the oracle.
+
+Layer bar (bf16-rounded inputs against the oracle): max|d| <= 1e-2 max|ref| and
+mean|d| / mean|ref| <= 5e-3.  Routing inside the layer: the GPU's fp32 logits are routed
+by the oracle and must select the same experts (near ties excluded and counted); the
+logits themselves must match the oracle's router linear within 1e-5 of max|logit|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_moe_layer_gb300 import binding, inputs
+
+from support import (bits, check_layer, check_route, near_tie_rows, oracle_experts,
+                     oracle_shared)
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda")
+
+
+def _layer(w, data):
+    return binding.MoELayer(data["w_router"], data["bias"], data["experts"], data["shared"],
+                            w.top_k, w.n_group, w.topk_group, w.norm_topk_prob,
+                            w.routed_scaling_factor, data["logit_offset"])
+
+
+def _check_forward(w, data, rows=None, check_logits_rows=None):
+    """Runs the layer, checks routing on every row, logits and the output on `rows`."""
+    layer = _layer(w, data)
+    y, inds, scores, logits = layer(data["x"], want_intermediates=True)
+    torch.cuda.synchronize()
+    binding.device_status()
+    lg = logits.cpu().numpy()
+    bias = data["bias"].cpu().numpy()
+    ri, rs = oracle.route(lg, bias, w.top_k, w.n_group, w.topk_group, w.norm_topk_prob,
+                          w.routed_scaling_factor)
+    ties = near_tie_rows(lg, bias, w.top_k, w.n_group, w.topk_group)
+    n_ties = check_route(inds.cpu().numpy(), scores.cpu().numpy(), ri, rs, ties)
+    xb = bits(data["x"])
+    lrows = np.arange(w.T) if check_logits_rows is None else np.asarray(check_logits_rows)
+    off = None if data["logit_offset"] is None else data["logit_offset"].cpu().numpy()
+    ref_lg = oracle.router_logits(xb[lrows], bits(data["w_router"]), off)
+    assert np.abs(lg[lrows] - ref_lg).max() <= 1e-5 * np.abs(ref_lg).max()
+    rows = np.arange(w.T) if rows is None else np.asarray(rows)
+    rows = rows[~ties[rows]]
+    if data["experts"]["bits"] == 16 and w.E * w.I * w.d <= (1 << 26):
+        ex = oracle_experts(data["experts"])
+        sel_inds = ri
+    else:
+        # only the experts the sampled rows use, renumbered
+        used = np.unique(ri[rows])
+        remap = np.full(w.E, -1, np.int32)
+        remap[used] = np.arange(len(used), dtype=np.int32)
+        ex = oracle_experts(data["experts"], torch.as_tensor(used, device=DEV))
+        sel_inds = np.where(ri >= 0, remap[ri], -1)
+    ref = oracle.moe_layer(xb, sel_inds, rs, ex, oracle_shared(data["shared"]), rows=rows)
+    got = y.float().cpu().numpy()[rows]
+    tol = (1e-2, 5e-3) if data["experts"]["bits"] == 16 else (3e-2, 1e-2)
+    mx, mean = check_layer(got, ref, *tol)
+    return dict(ties=n_ties, max=mx, mean=mean, counts=np.bincount(ri.reshape(-1), minlength=w.E))
+
+
+def test_tiny_layer_all_tokens():
+    w = inputs.WORKLOADS["tiny_T64_E16"]
+    r = _check_forward(w, inputs.gen_layer(w, DEV, seed=0))
+    print(r)
+
+
+# T values that take each token-tile choice of the expert GEMMs (16/32/64 tokens on N,
+# 128-token tiles on M) and of the router (tokens on N up to 256, on M above), with
+# ragged tails everywhere.
+@pytest.mark.parametrize("T", [1, 5, 33, 96, 150, 300, 520])
+def test_layer_token_tiles(T):
+    w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=T)
+    _check_forward(w, inputs.gen_layer(w, DEV, seed=T))
+
+
+@pytest.mark.parametrize("T,d,I,E,K,G,tg", [
+    (300, 512, 384, 32, 4, 4, 2),      # several feature tiles, d not a multiple of 256 tiles
+    (40, 384, 256, 8, 2, 2, 1),        # d = 3 x 128
+    (700, 640, 128, 24, 6, 3, 2),      # many 128-token tiles, uneven experts
+])
+def test_layer_multi_tile(T, d, I, E, K, G, tg):
+    w = inputs.Workload("mt", T=T, d=d, E=E, I=I, top_k=K, n_group=G, topk_group=tg,
+                        norm_topk_prob=True, routed_scaling_factor=2.5, bias_var=0.05)
+    _check_forward(w, inputs.gen_layer(w, DEV, seed=1))
+
+
+def test_layer_without_shared_expert():
+    w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=100, shared=False)
+    _check_forward(w, inputs.gen_layer(w, DEV, seed=2))
+
+
+def test_layer_skewed_routing():
+    w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=400, zipf=True)
+    r = _check_forward(w, inputs.gen_layer(w, DEV, seed=3))
+    assert r["counts"].max() > 4 * r["counts"].mean()
+
+
+def test_parts_router_swiglu_combine():
+    w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=77)
+    data = inputs.gen_layer(w, DEV, seed=4)
+    x = data["x"]
+    lg = binding.router_logits(x, data["w_router"])
+    lg_off = binding.router_logits(x, data["w_router"], data["bias"])
+    inds, scores = binding.route_deepseek(lg, data["bias"], w.top_k, w.n_group, w.topk_group,
+                                          w.norm_topk_prob, w.routed_scaling_factor)
+    counts, offsets, perm, inv = binding.permute(inds, w.E)
+    eo = binding.grouped_swiglu(x, offsets, perm, w.top_k, data["experts"], data["shared"])
+    P = w.T * w.top_k
+    y = binding.combine(eo[:P], scores, inv, eo[P:])
+    torch.cuda.synchronize()
+    xb = bits(x)
+    ref_lg = oracle.router_logits(xb, bits(data["w_router"]))
+    assert np.abs(lg.cpu().numpy() - ref_lg).max() <= 1e-5 * np.abs(ref_lg).max()
+    ref_off = oracle.router_logits(xb, bits(data["w_router"]), data["bias"].cpu().numpy())
+    assert np.abs(lg_off.cpu().numpy() - ref_off).max() <= 1e-5 * np.abs(ref_off).max()
+    ii, ss = inds.cpu().numpy(), scores.cpu().numpy()
+    ex = oracle_experts(data["experts"])
+    # expert rows in slot order: slot j holds pair perm[j] = t*K + k
+    pp = perm.cpu().numpy()
+    one = np.ones((w.T, 1), np.float32)
+    for j in range(0, P, 37):
+        t, k = divmod(int(pp[j]), w.top_k)
+        ref = oracle.moe_layer(xb, ii[:, k:k + 1], one, ex, None, rows=[t])
+        check_layer(eo[j:j + 1].float().cpu().numpy(), ref)
+    ref_sh = oracle.moe_layer(xb, ii[:, :1], np.zeros((w.T, 1), np.float32), ex,
+                              oracle_shared(data["shared"]))
+    check_layer(eo[P:].float().cpu().numpy(), ref_sh)
+    ref = oracle.moe_layer(xb, ii, ss, ex, oracle_shared(data["shared"]))
+    check_layer(y.float().cpu().numpy(), ref)
+
+
+def test_layer_empty_batch():
+    w = inputs.WORKLOADS["tiny_T64_E16"]
+    data = inputs.gen_layer(w, DEV, seed=0)
+    layer = _layer(w, data)
+    y = layer(data["x"][:0])
+    torch.cuda.synchronize()
+    assert y.shape == (0, w.d)
+
+
+# ------------------------------------------------------------------------------------
+# DeepSeek-V3-shaped layers at full size, outputs checked on sampled tokens
+# ------------------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def dsv3_weights():
+    w = inputs.WORKLOADS["dsv3_T128"]
+    data = inputs.gen_layer(w, DEV, seed=0)
+    yield data
+    del data
+    torch.cuda.empty_cache()
+
+
+def test_dsv3_decode_T128(dsv3_weights):
+    w = inputs.WORKLOADS["dsv3_T128"]
+    r = _check_forward(w, dsv3_weights, rows=[0, 37, 90, 127])
+    print(r["ties"], r["max"], r["mean"], int((r["counts"] > 0).sum()))
+
+
+def test_dsv3_prefill_T8192_zipf(dsv3_weights):
+    w = inputs.WORKLOADS["dsv3_T8192_zipf"]
+    data = dict(dsv3_weights)
+    data["x"] = inputs.gen_tokens(w, DEV, seed=0)
+    data["logit_offset"] = inputs.zipf_offsets(w.E, DEV, 0)
+    r = _check_forward(w, data, rows=[0, 4095, 8191], check_logits_rows=np.arange(0, 8192, 97))
+    print(r["ties"], r["max"], r["mean"], int((r["counts"] > 0).sum()), int(r["counts"].max()))
