@@ -278,7 +278,7 @@ int moe_route_deepseek(const void* logits, moe_dtype_t dtype, int64_t rows, int3
                        const float* bias, const moe_route_params_t* params, int32_t* inds,
                        float* scores, moe_stream_t stream) {
     g_err.clear();
-    MOE_CHECK(logits && bias && inds && scores, "NULL pointer argument");
+    MOE_CHECK(bias && (rows == 0 || (logits && inds && scores)), "NULL pointer argument");
     MOE_CHECK(dtype == MOE_DTYPE_F32 || dtype == MOE_DTYPE_BF16, "dtype %d unknown", (int)dtype);
     MOE_CHECK(rows >= 0, "rows = %lld < 0", (long long)rows);
     int rc = check_route_params(E, params);
@@ -310,7 +310,8 @@ int moe_route_deepseek(const void* logits, moe_dtype_t dtype, int64_t rows, int3
 int moe_permute(const int32_t* inds, int64_t T, int32_t K, int32_t E, int32_t* counts,
                 int32_t* offsets, int32_t* perm, int32_t* inv_perm, moe_stream_t stream) {
     g_err.clear();
-    MOE_CHECK(inds && counts && offsets && perm && inv_perm, "NULL pointer argument");
+    MOE_CHECK(counts && offsets && (T * (int64_t)K == 0 || (inds && perm && inv_perm)),
+              "NULL pointer argument");
     MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
     MOE_CHECK(K >= 1, "K = %d < 1", K);
     MOE_CHECK(E >= 1 && E <= kMaxExperts, "E = %d outside [1, %d]", E, kMaxExperts);
@@ -326,7 +327,7 @@ int moe_permute(const int32_t* inds, int64_t T, int32_t K, int32_t E, int32_t* c
 int moe_router_logits(const void* x, int64_t T, int32_t d, const void* w_router, int32_t E,
                       const float* logit_offset, float* logits, moe_stream_t stream) {
     g_err.clear();
-    MOE_CHECK(x && w_router && logits, "NULL pointer argument");
+    MOE_CHECK(w_router && (T == 0 || (x && logits)), "NULL pointer argument");
     MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
     MOE_CHECK(d >= 64 && d % 64 == 0, "d = %d must be a positive multiple of 64", d);
     MOE_CHECK(E >= 1 && E <= kMaxExperts, "E = %d outside [1, %d]", E, kMaxExperts);
@@ -372,7 +373,7 @@ int moe_grouped_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E
                        const moe_expert_weights_t* experts, const moe_expert_weights_t* shared,
                        void* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
     g_err.clear();
-    MOE_CHECK(x && offsets && perm && out && ws, "NULL pointer argument");
+    MOE_CHECK(offsets && ws && (T == 0 || (x && perm && out)), "NULL pointer argument");
     int rc = check_dims(T, d, I, E, K);
     if (rc) return rc;
     rc = check_weights(experts, "expert", 0);
@@ -396,7 +397,7 @@ int moe_combine(const void* expert_out, const float* scores, const int32_t* inv_
                 const void* shared_out, int64_t T, int32_t K, int32_t d, void* y,
                 moe_stream_t stream) {
     g_err.clear();
-    MOE_CHECK(expert_out && scores && inv_perm && y, "NULL pointer argument");
+    MOE_CHECK(T == 0 || (expert_out && scores && inv_perm && y), "NULL pointer argument");
     MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
     MOE_CHECK(K >= 1, "K = %d < 1", K);
     MOE_CHECK(d >= 8 && d % 8 == 0, "d = %d must be a positive multiple of 8", d);
@@ -424,7 +425,7 @@ int moe_forward(const void* x, int64_t T, int32_t d, int32_t I, int32_t E,
                 float* scores_out, float* logits_out, void* ws, size_t ws_bytes,
                 moe_stream_t stream) {
     g_err.clear();
-    MOE_CHECK(x && w_router && bias && y && ws, "NULL pointer argument");
+    MOE_CHECK(w_router && bias && ws && (T == 0 || (x && y)), "NULL pointer argument");
     int rc = check_route_params(E, params);
     if (rc) return rc;
     const int32_t K = params->top_k;

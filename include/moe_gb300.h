@@ -16,6 +16,8 @@
  *   - Every tensor pointer is a DEVICE pointer on the current CUDA device, unless the
  *     argument says otherwise; the caller owns all memory (outputs and workspaces too).
  *     Row-major layouts throughout; bf16 is IEEE bfloat16, fp16 is IEEE binary16.
+ *   - A call with zero tokens (T == 0 / rows == 0) launches nothing except moe_permute,
+ *     which still writes counts and offsets; its token-sized arrays may then be NULL.
  *   - Every call is asynchronous on `stream` (NULL = the legacy default stream) and
  *     never synchronises the host, except moe_device_status().
  *   - Return value: MOE_OK (0) or a negative code.  All argument checks run on the host

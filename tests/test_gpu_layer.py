@@ -96,7 +96,7 @@ def test_layer_without_shared_expert():
 def test_layer_skewed_routing():
     w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=400, zipf=True)
     r = _check_forward(w, inputs.gen_layer(w, DEV, seed=3))
-    assert r["counts"].max() > 4 * r["counts"].mean()
+    assert r["counts"].max() > 3 * r["counts"].mean() and (r["counts"] <= 1).any()
 
 
 def test_parts_router_swiglu_combine():
