@@ -35,9 +35,18 @@ from deepseek_moe_layer_gb300 import binding, inputs  # noqa: E402
 METRIC = "MoE-layer tokens/s (DSv3 shape, T=128 & T=8192); % of HBM/tensor roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic (read + write bytes per launch) of the dominant kernel from an ncu capture,
-# keyed by workload, with the hash of the GEMM sources it was taken on; stale -> null.
-NCU_TRAFFIC = {}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant kernel per
+# algorithmic byte, from an ncu capture of a reduced case of the same shapes (the full
+# workloads are too large to replay); traffic grows with the expert bytes processed, so the
+# per-launch traffic of the full workload is ratio x its algorithmic bytes.  Keyed by
+# workload with the hash of the GEMM sources the capture ran; a stale hash reports null.
+# Captures: profiles/moe_gemm_gateup_dsv3_E32_T16.md, moe_gemm_gateup_dsv3_E32_T1024_zipf.md.
+NCU_TRAFFIC = {
+    "dsv3_T128": {"src": "c11937a8340574d2", "ratio": (1.705243e9 + 3.266304e6) / 1705541632},
+    "dsv3_T8192_zipf": {"src": "c11937a8340574d2",
+                        "ratio": (2.110998e9 + 27.3088e6) / (32 * 2 * 2048 * 7168 * 2
+                                                             + 9216 * (7168 + 2048) * 2)},
+}
 
 
 def kernel_source_hash():
@@ -58,7 +67,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    """nvidia-smi clock / throttle-reason samples every 100 ms while running."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -78,7 +87,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
                 stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -238,7 +247,8 @@ def kernel_roofline(w, t, alg, peaks, src):
     t_hbm = alg["gate_up_bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_tc = alg["gate_up_flops"] / (peaks["bf16_tflops_sustained"] * 1e12)
     tr = NCU_TRAFFIC.get(w.name)
-    traffic = tr["bytes"] if tr and tr.get("src") == src else None
+    traffic = (int(tr["ratio"] * alg["gate_up_bytes"])
+               if tr and tr.get("src") == src else None)
     if t_hbm >= t_tc:
         r = roofline("hbm", alg["gate_up_bytes"] / sec, peaks, True, traffic)
         r["algorithmic"] = alg["gate_up_bytes"]
@@ -346,17 +356,21 @@ def run_ours(args):
     src = kernel_source_hash()
 
     w, data = workload_data(args.workload, dev)
+    do_pre = bool(args.prefill) and w.d == inputs.WORKLOADS[args.prefill].d and \
+        w.E == inputs.WORKLOADS[args.prefill].E and w.bits == inputs.WORKLOADS[args.prefill].bits
+    if do_pre:
+        wp, dp = workload_data(args.prefill, dev, base=data)
     sampler = ClockSampler(dev)
-    with sampler:
+    with sampler:  # clocks sampled across both timed loops
         t = time_layer(w, data, args.steps, args.warmup, dev)
+        if do_pre:
+            tp = time_layer(wp, dp, args.steps, args.warmup, dev)
     clocks = sampler.summary()
     e2e = time_e2e(w, data, args.steps, args.warmup, dev)
     alg = algorithmic(w, t["counts"])
 
     pre = None
-    if args.prefill and not args.workload.startswith("tiny"):
-        wp, dp = workload_data(args.prefill, dev, base=data)
-        tp = time_layer(wp, dp, args.steps, args.warmup, dev)
+    if do_pre:
         algp = algorithmic(wp, tp["counts"])
         pre = {"workload": wp.name, "T": wp.T, "value": round(wp.T / (tp["ms"] / 1e3), 1),
                "unit": "tokens/s", "ms_per_step": round(tp["ms"], 4),
@@ -447,7 +461,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv3_T128", choices=sorted(inputs.WORKLOADS))
