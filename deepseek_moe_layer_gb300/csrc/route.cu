@@ -44,7 +44,36 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteArgs a) {
     for (int i = 0; i < EPL; ++i) lg[i] = 0.0f;
     if (!a.bf16) {
         const float* base = static_cast<const float*>(a.logits) + row * E;
-        for (int s = 0; s < a.nsplit; ++s) {
+        int s0 = 0;
+        if constexpr (EPL % 4 == 0) {
+            // batches of 8 splits: all loads issued before the (in-order) additions
+            const bool vec = (E & 3) == 0 && (reinterpret_cast<uintptr_t>(base) & 15) == 0 &&
+                             (a.split_stride & 3) == 0;
+            if (vec && e0 < E) {
+                for (; s0 + 8 <= a.nsplit; s0 += 8) {
+                    float4 v[8][EPL / 4];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+#pragma unroll
+                        for (int i = 0; i < EPL / 4; ++i)
+                            v[u][i] = (e0 + 4 * i < E)  // E % 4 == 0: a vector is all in or out
+                                          ? *reinterpret_cast<const float4*>(
+                                                base + (long long)(s0 + u) * a.split_stride +
+                                                e0 + 4 * i)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+#pragma unroll
+                        for (int i = 0; i < EPL / 4; ++i) {
+                            lg[4 * i] += v[u][i].x;
+                            lg[4 * i + 1] += v[u][i].y;
+                            lg[4 * i + 2] += v[u][i].z;
+                            lg[4 * i + 3] += v[u][i].w;
+                        }
+                }
+            }
+        }
+        for (int s = s0; s < a.nsplit; ++s) {
             const float* p = base + (long long)s * a.split_stride;
             if constexpr (EPL % 4 == 0) {
                 if ((E & 3) == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
