@@ -23,7 +23,7 @@ MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
 EXPORTS = ("moe_last_error", "moe_version", "moe_device_status", "moe_route_deepseek",
            "moe_permute", "moe_router_logits", "moe_grouped_swiglu",
            "moe_grouped_swiglu_workspace_bytes", "moe_combine", "moe_forward",
-           "moe_forward_workspace_bytes", "moe_set_phase_events")
+           "moe_forward_workspace_bytes", "moe_set_phase_events", "moe_forward_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -79,9 +79,13 @@ def lib(path: str | None = None):
             L.moe_forward_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32]
             L.moe_forward_workspace_bytes.restype = sz
             L.moe_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
+            L.moe_forward_noalloc.argtypes = [P, i64, i32, i32, i32, P, P, P,
+                                              ctypes.POINTER(RouteParams),
+                                              ctypes.POINTER(ExpertWeights),
+                                              ctypes.POINTER(ExpertWeights), P, P, P, P, P]
             for name in ("moe_device_status", "moe_route_deepseek", "moe_permute",
                          "moe_router_logits", "moe_grouped_swiglu", "moe_combine",
-                         "moe_forward", "moe_set_phase_events"):
+                         "moe_forward", "moe_set_phase_events", "moe_forward_noalloc"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib

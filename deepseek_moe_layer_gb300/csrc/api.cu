@@ -259,6 +259,11 @@ int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_
 
 }  // namespace
 
+int moe::set_error(int code, const char* msg) {
+    g_err = msg;
+    return code;
+}
+
 extern "C" {
 
 const char* moe_last_error(void) { return g_err.c_str(); }

@@ -84,4 +84,7 @@ cudaError_t read_device_status(unsigned int* out, int clear, cudaStream_t s);
 
 int num_sms();
 
+// Sets the thread-local text returned by moe_last_error() and returns `code`.
+int set_error(int code, const char* msg);
+
 }  // namespace moe

@@ -193,6 +193,32 @@ size_t moe_forward_workspace_bytes(int64_t T, int32_t d, int32_t I, int32_t E, i
                                    int32_t has_shared);
 
 /*
+ * moe_forward_noalloc -- moe_forward without a caller workspace.  The pages have no
+ * counterpart: it exists for callers that cannot allocate device memory — serving engines
+ * that reserve nearly all of HBM for their own pools, code running under CUDA stream
+ * capture (where cudaMalloc is not allowed), hosts whose allocator belongs to another
+ * framework.  Arguments and results are those of moe_forward minus ws / ws_bytes.
+ *   - The workspace is a fixed array of MOE_NOALLOC_SCRATCH_BYTES (64 MiB) in the
+ *     library's own device memory, held on every device that loads the library until the
+ *     process exits; it fits decode batches (up to about 169 tokens at d = 7168, E = 256,
+ *     I = 2048, top_k = 8 with a shared expert).  A layer whose
+ *     moe_forward_workspace_bytes() exceeds it is rejected with MOE_ERR_INVALID before
+ *     anything runs.
+ *   - The first call on a device resolves the array's address with that device current;
+ *     make that first call before any stream capture.
+ *   - All calls on a device share the array: calls that overlap on the GPU race, so keep
+ *     them on one stream.  The array keeps the last call's contents; nothing in it needs
+ *     to start at zero.
+ *   - Allocates nothing: no cudaMalloc / cudaFree and no allocating library routine.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int moe_forward_noalloc(const void* x, int64_t T, int32_t d, int32_t I, int32_t E,
+                        const void* w_router, const float* bias, const float* logit_offset,
+                        const moe_route_params_t* params, const moe_expert_weights_t* experts,
+                        const moe_expert_weights_t* shared, void* y, int32_t* inds_out,
+                        float* scores_out, float* logits_out, moe_stream_t stream);
+
+/*
  * moe_set_phase_events -- a timing aid with no counterpart in the pages: while set,
  * moe_forward records events[i] on its stream at the boundaries of its steps:
  *   0 start, 1 after the router linear, 2 after the gate, 3 after the dispatch,
