@@ -369,16 +369,31 @@ def run_ours(args):
     e2e = time_e2e(w, data, args.steps, args.warmup, dev)
     alg = algorithmic(w, t["counts"])
 
+    def summary(wx, tx):
+        algx = algorithmic(wx, tx["counts"])
+        return {"workload": wx.name, "T": wx.T, "expert_bits": wx.bits,
+                "value": round(wx.T / (tx["ms"] / 1e3), 1),
+                "unit": "tokens/s", "ms_per_step": round(tx["ms"], 4),
+                "phases_ms": {k: round(v, 4) for k, v in tx["phases"].items()},
+                "experts_hit": algx["experts_hit"], "max_expert_load": int(tx["counts"].max()),
+                "roofline": kernel_roofline(wx, tx, algx, peaks, src),
+                "layer_roofline": layer_roofline(algx, tx["ms"], peaks)}
+
     pre = None
     if do_pre:
-        algp = algorithmic(wp, tp["counts"])
-        pre = {"workload": wp.name, "T": wp.T, "value": round(wp.T / (tp["ms"] / 1e3), 1),
-               "unit": "tokens/s", "ms_per_step": round(tp["ms"], 4),
-               "phases_ms": {k: round(v, 4) for k, v in tp["phases"].items()},
-               "experts_hit": algp["experts_hit"], "max_expert_load": int(tp["counts"].max()),
-               "roofline": kernel_roofline(wp, tp, algp, peaks, src),
-               "layer_roofline": layer_roofline(algp, tp["ms"], peaks)}
+        pre = summary(wp, tp)
         del dp
+    # the affine 4-bit expert workloads (decode T=32, prefill T=4096 with Zipf routing)
+    q4 = {}
+    if args.q4 and w.d == 7168 and w.E == 256:
+        wq, dq = workload_data("dsv3_q4_T32", dev)
+        tq = time_layer(wq, dq, args.steps, args.warmup, dev)
+        q4["q4_decode"] = summary(wq, tq)
+        wq2, dq2 = workload_data("dsv3_q4_T4096_zipf", dev, base=dq)
+        tq2 = time_layer(wq2, dq2, args.steps, args.warmup, dev)
+        q4["q4_prefill"] = summary(wq2, tq2)
+        del dq, dq2
+        torch.cuda.empty_cache()
 
     # aggregate over ranks: tokens of all ranks / max time
     tot = torch.tensor([t["total_ms"], e2e["ms"]], dtype=torch.float64)
@@ -413,6 +428,7 @@ def run_ours(args):
     }
     if pre is not None:
         line["prefill"] = pre
+    line.update(q4)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, data)
     if rank == 0:
@@ -467,6 +483,8 @@ def main():
     ap.add_argument("--workload", default="dsv3_T128", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--prefill", default="dsv3_T8192_zipf")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-q4", dest="q4", action="store_false",
+                    help="skip the affine 4-bit expert workloads")
     args = ap.parse_args()
     if args.prefill in ("", "none"):
         args.prefill = None

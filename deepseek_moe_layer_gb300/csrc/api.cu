@@ -106,8 +106,10 @@ int check_weights(const moe_expert_weights_t* w, const char* what, int shared) {
         MOE_CHECK(w->gate_scale && w->gate_bias && w->up_scale && w->up_bias && w->down_scale &&
                       w->down_bias,
                   "%s weights: 4-bit scale/bias pointer is NULL", what);
-        return fail(MOE_ERR_INVALID, "%s weights: the affine 4-bit path is not available in "
-                                     "this build", what);
+        MOE_CHECK(aligned(w->gate_scale, 2) && aligned(w->gate_bias, 2) &&
+                      aligned(w->up_scale, 2) && aligned(w->up_bias, 2) &&
+                      aligned(w->down_scale, 2) && aligned(w->down_bias, 2),
+                  "%s weights: fp16 scale/bias pointers must be 2-byte aligned", what);
     }
     return MOE_OK;
 }

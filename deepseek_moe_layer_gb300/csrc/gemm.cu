@@ -56,7 +56,9 @@ __host__ __device__ constexpr int pow2ceil(int v) {
     return p;
 }
 
-template <int MODE, int TOKT>
+constexpr int kDequantWarps = 8;  // 4-bit variant: warps turning packed codes into bf16
+
+template <int MODE, int TOKT, bool Q4>
 struct Cfg {
     static constexpr bool kSwap = TOKT != 0;
     static constexpr int kTok = kSwap ? TOKT : 128;                  // tokens per tile
@@ -65,7 +67,9 @@ struct Cfg {
     static constexpr int kFeat = kSwap ? 128 : (MODE == kGateUp ? 128 : 256);
     static constexpr int kXBytes = kTok * 128;
     static constexpr int kWBytes = kWRows * 128;
-    static constexpr int kStageBytes = kXBytes + kWBytes;
+    static constexpr int kRBytes = Q4 ? kWRows * 32 : 0;  // packed codes: 8 words per row
+    static constexpr int kStageBytes = kXBytes + kWBytes + kRBytes;
+    static constexpr int kThreadsCta = Q4 ? kThreads + 32 * kDequantWarps : kThreads;
     static constexpr int kStages = cmin(12, (200 * 1024) / kStageBytes);
     static constexpr int kAccCols = kSwap ? kTok * kNW : 256;
     static constexpr int kTmemCols = pow2ceil(cmax(32, 2 * kAccCols));
@@ -74,7 +78,7 @@ struct Cfg {
     static constexpr int kMaxGroups = 1025;
     // shared memory: stages | barriers | misc | tile prefix | row offsets
     static constexpr int kBarOff = kStages * kStageBytes;
-    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kNumBars = 3 * kStages + 5;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kPrefixOff = kMiscOff + 16;
     static constexpr int kRowOffOff = kPrefixOff + 4 * (kMaxGroups + 1);
@@ -98,7 +102,38 @@ struct KParams {
     long long split_stride;
     void* out;
     long long out_ld;
+    // 4-bit weights: fp16 scale / bias per group of 64 inputs, [rows_total, Kdim / 64]
+    const unsigned short* qscale[2];
+    const unsigned short* qbias[2];
 };
+
+// Eight packed 4-bit codes (element j in bits 4j..4j+3 of the word) -> eight bf16 weights
+// w = scale * q + bias, as four bf16x2 words in element order.  Each code becomes the bf16
+// number 128 + q exactly (0x43 exponent byte over the code), 128 is subtracted exactly, and
+// one fused bf16x2 multiply-add applies the group's scale and bias (one rounding).
+MOE_DEV uint4 dequant8(uint32_t w, uint32_t s2, uint32_t b2) {
+    const uint32_t t0 = w & 0x0F0F0F0Fu;          // codes 0, 2, 4, 6, one per byte
+    const uint32_t t1 = (w >> 4) & 0x0F0F0F0Fu;   // codes 1, 3, 5, 7
+    const uint32_t lo = __byte_perm(t0, t1, 0x5140);  // codes 0, 1, 2, 3
+    const uint32_t hi = __byte_perm(t0, t1, 0x7362);  // codes 4, 5, 6, 7
+    uint32_t v[4];
+    v[0] = __byte_perm(lo, 0x43u, 0x4140);  // bf16 pair (128 + c0, 128 + c1)
+    v[1] = __byte_perm(lo, 0x43u, 0x4342);
+    v[2] = __byte_perm(hi, 0x43u, 0x4140);
+    v[3] = __byte_perm(hi, 0x43u, 0x4342);
+    uint32_t r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t q;
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(v[i]), "r"(0x43004300u));
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r[i]) : "r"(q), "r"(s2), "r"(b2));
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+MOE_DEV void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 struct TileInfo {
     int g;               // group (E = shared)
@@ -165,22 +200,25 @@ MOE_DEV void record_timeout(volatile int* abort) {
     atomicCAS(&g_status, 0u, kStatusTimeout);
 }
 
-template <int MODE, int TOKT>
-__global__ void __launch_bounds__(kThreads, 1)
+// tm_w0 / tm_w1: bf16 weight rows (Q4 = false) or packed 4-bit code rows (Q4 = true); the
+// shared expert's maps tm_sw0 / tm_sw1 are always bf16.
+template <int MODE, int TOKT, bool Q4>
+__global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
                     const __grid_constant__ CUtensorMap tm_act_sh,
                     const __grid_constant__ CUtensorMap tm_w0,
                     const __grid_constant__ CUtensorMap tm_w1,
                     const __grid_constant__ CUtensorMap tm_sw0,
                     const __grid_constant__ CUtensorMap tm_sw1, const KParams p) {
-    using C = Cfg<MODE, TOKT>;
+    using C = Cfg<MODE, TOKT, Q4>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::kStages;
-    uint64_t* tfull = bars + 2 * C::kStages;
+    uint64_t* rawfull = bars + 2 * C::kStages;  // 4-bit: packed codes of the stage landed
+    uint64_t* tfull = bars + 3 * C::kStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* done = tfull + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
@@ -195,8 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- set-up: barriers, TMEM, group offsets and the tile prefix ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], Q4 ? 1 + kDequantWarps : 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&rawfull[s], 1);
         }
         mbar_init(&tfull[0], 1);
         mbar_init(&tfull[1], 1);
@@ -214,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
     if (p.offsets)
-        for (int i = threadIdx.x; i <= p.E; i += kThreads) rowoff[i] = p.offsets[i];
+        for (int i = threadIdx.x; i <= p.E; i += blockDim.x) rowoff[i] = p.offsets[i];
     __syncthreads();
     if (warp == 0) {
         const int per = (ngroups + 31) / 32;
@@ -258,23 +297,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
                     uint8_t* st = smem + s * C::kStageBytes;
-                    mbar_arrive_expect_tx(&full[s], C::kStageBytes);
                     const int kx = kb * kBK;
-                    tma_load_2d(st, am, &full[s], kx, (int)ti.act_row, pol_x);
                     uint8_t* wst = st + C::kXBytes;
+                    if (Q4 && !ti.shared) {
+                        // token rows -> full[s]; packed codes -> rawfull[s] (the dequant
+                        // warps complete full[s] once the bf16 weights are in place)
+                        mbar_arrive_expect_tx(&full[s], C::kXBytes);
+                        tma_load_2d(st, am, &full[s], kx, (int)ti.act_row, pol_x);
+                        uint8_t* rst = wst + C::kWBytes;
+                        mbar_arrive_expect_tx(&rawfull[s], C::kRBytes);
+                        if (MODE == kGateUp) {
+                            tma_load_2d(rst, w0, &rawfull[s], kb * 8, wrow, pol_w);
+                            tma_load_2d(rst + 128 * 32, w1, &rawfull[s], kb * 8, wrow, pol_w);
+                        } else {
+                            tma_load_2d(rst, w0, &rawfull[s], kb * 8, wrow, pol_w);
+                        }
+                        continue;
+                    }
+                    mbar_arrive_expect_tx(&full[s], C::kXBytes + C::kWBytes);
+                    tma_load_2d(st, am, &full[s], kx, (int)ti.act_row, pol_x);
                     if (MODE == kGateUp) {
                         tma_load_2d(wst, w0, &full[s], kx, wrow, pol_w);
                         tma_load_2d(wst + 128 * 128, w1, &full[s], kx, wrow, pol_w);
                     } else {
                         tma_load_2d(wst, w0, &full[s], kx, wrow, pol_w);
                     }
+                    if (Q4) mbar_arrive(&rawfull[s]);  // bf16 shared expert: nothing to dequantise
                 }
             }
             if (!ok) {
                 // let the copies already issued land before the CTA can exit
-                for (int n = (it > C::kStages ? it - C::kStages : 0); n < it; ++n)
-                    mbar_wait(&full[n % C::kStages], (uint32_t)(n / C::kStages) & 1u, nullptr,
-                              100000000ull);
+                for (int n = (it > C::kStages ? it - C::kStages : 0); n < it; ++n) {
+                    const uint32_t par = (uint32_t)(n / C::kStages) & 1u;
+                    if (Q4) mbar_wait(&rawfull[n % C::kStages], par, nullptr, 100000000ull);
+                    mbar_wait(&full[n % C::kStages], par, nullptr, 100000000ull);
+                }
             }
         }
     } else if (warp == 1) {
@@ -320,6 +377,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it > 0) {
                 umma_commit(done);
                 mbar_wait(done, 0u, nullptr, 100000000ull);
+            }
+        }
+    } else if (Q4 && warp >= kThreads / 32) {
+        // ============================ 4-bit dequantisation ==========================
+        // 256 threads; thread dt owns row dt % kWRows of the stage's weight tile and
+        // kWordsPT of its 8 packed words (one 64-element k-block = one scale group).
+        constexpr int kWordsPT = C::kWRows * 8 / (32 * kDequantWarps);
+        const int dt = threadIdx.x - kThreads;
+        const int r = dt % C::kWRows;
+        const int wd0 = (dt / C::kWRows) * kWordsPT;
+        const int mat = (MODE == kGateUp && r >= 128) ? 1 : 0;
+        const int rr = (MODE == kGateUp) ? (r & 127) : r;
+        const unsigned short* sp = mat ? p.qscale[1] : p.qscale[0];
+        const unsigned short* bp = mat ? p.qbias[1] : p.qbias[0];
+        const int kgroups = p.Kdim / kBK;
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
+            const bool rvalid = !ti.shared && ti.f * C::kFeat + rr < p.F;
+            const long long grow = (long long)ti.g * p.F + ti.f * C::kFeat + rr;
+            for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++it) {
+                const int s = it % C::kStages;
+                const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
+                unsigned short sb = 0, bb = 0;  // fp16 bits of this row's scale and bias
+                if (rvalid) {
+                    sb = __ldg(sp + grow * kgroups + kb);
+                    bb = __ldg(bp + grow * kgroups + kb);
+                }
+                if (!mbar_wait(&rawfull[s], ph, abort)) { record_timeout(abort); ok = false; break; }
+                if (!ti.shared) {
+                    const float sf = __half2float(__ushort_as_half(sb));
+                    const float bf = __half2float(__ushort_as_half(bb));
+                    const uint32_t s2 = pack_bf16x2(sf, sf), b2 = pack_bf16x2(bf, bf);
+                    uint8_t* st = smem + s * C::kStageBytes;
+                    const uint8_t* rrow = st + C::kXBytes + C::kWBytes + r * 32;
+                    uint8_t* wrow_s = st + C::kXBytes + r * 128;
+                    uint32_t words[kWordsPT];
+#pragma unroll
+                    for (int v = 0; v < kWordsPT / 4; ++v) {
+                        const uint4 q4 = *reinterpret_cast<const uint4*>(rrow + (wd0 + 4 * v) * 4);
+                        words[4 * v] = q4.x; words[4 * v + 1] = q4.y;
+                        words[4 * v + 2] = q4.z; words[4 * v + 3] = q4.w;
+                    }
+#pragma unroll
+                    for (int w = 0; w < kWordsPT; ++w) {
+                        const int c = wd0 + w;  // 16-byte chunk = 8 elements of the row
+                        *reinterpret_cast<uint4*>(wrow_s + ((c ^ (r & 7)) << 4)) =
+                            dequant8(words[w], s2, b2);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[s]);
             }
         }
     } else {
@@ -484,13 +595,30 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int TOKT>
+// 2-D uint32 tensor [rows, cols_u32] of packed 4-bit codes, box of 8 words (64 codes) x
+// box_rows rows, no swizzle (the dequant warps read it row by row).
+bool make_map_q4(CUtensorMap* m, const void* base, long long rows, long long cols_u32,
+                 int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    if (rows < 1) rows = 1;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols_u32, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols_u32 * 4};
+    const cuuint32_t box[2] = {8u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE, int TOKT, bool Q4>
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
-    using C = Cfg<MODE, TOKT>;
+    using C = Cfg<MODE, TOKT, Q4>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, TOKT>,
+        attr_err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, TOKT, Q4>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::kSmemBytes);
     });
@@ -503,11 +631,17 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
     ok = ok && make_map(&m_act_sh, a.act_shared ? a.act_shared : a.act,
                         a.act_shared ? (a.shared_act_row0 + a.shared_rows) : a.act_rows, a.Kdim,
                         C::kTok);
-    ok = ok && make_map(&m_w0, a.w.w0, wrows_routed, a.Kdim, wbox);
-    ok = ok && make_map(&m_w1, a.w.w1 ? a.w.w1 : a.w.w0, wrows_routed, a.Kdim, wbox);
-    const void* sw0 = a.has_shared ? a.ws.w0 : a.w.w0;
-    const void* sw1 = a.has_shared ? (a.ws.w1 ? a.ws.w1 : a.ws.w0) : a.w.w0;
-    const long long srows = a.has_shared ? a.F : wrows_routed;
+    if (Q4) {
+        ok = ok && make_map_q4(&m_w0, a.w.w0, wrows_routed, a.Kdim / 8, wbox);
+        ok = ok && make_map_q4(&m_w1, a.w.w1 ? a.w.w1 : a.w.w0, wrows_routed, a.Kdim / 8, wbox);
+    } else {
+        ok = ok && make_map(&m_w0, a.w.w0, wrows_routed, a.Kdim, wbox);
+        ok = ok && make_map(&m_w1, a.w.w1 ? a.w.w1 : a.w.w0, wrows_routed, a.Kdim, wbox);
+    }
+    // shared expert maps are bf16 (a stand-in view of the act tensor when there is none)
+    const void* sw0 = a.has_shared ? a.ws.w0 : a.act;
+    const void* sw1 = a.has_shared ? (a.ws.w1 ? a.ws.w1 : a.ws.w0) : a.act;
+    const long long srows = a.has_shared ? a.F : a.act_rows;
     ok = ok && make_map(&m_sw0, sw0, srows, a.Kdim, wbox);
     ok = ok && make_map(&m_sw1, sw1, srows, a.Kdim, wbox);
     if (!ok) return cudaErrorInvalidValue;
@@ -526,23 +660,27 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
     p.split_stride = a.split_stride;
     p.out = a.out;
     p.out_ld = a.out_ld;
+    p.qscale[0] = static_cast<const unsigned short*>(a.w.s0);
+    p.qbias[0] = static_cast<const unsigned short*>(a.w.b0);
+    p.qscale[1] = static_cast<const unsigned short*>(a.w.s1);
+    p.qbias[1] = static_cast<const unsigned short*>(a.w.b1);
 
     long long grid = num_sms();
     if (a.max_tiles < grid) grid = a.max_tiles;
     if (grid < 1) return cudaSuccess;
-    moe_gemm_kernel<MODE, TOKT><<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(
+    moe_gemm_kernel<MODE, TOKT, Q4><<<(unsigned)grid, C::kThreadsCta, C::kSmemBytes, s>>>(
         m_act, m_act_sh, m_w0, m_w1, m_sw0, m_sw1, p);
     return cudaGetLastError();
 }
 
-template <int MODE>
+template <int MODE, bool Q4>
 cudaError_t dispatch_tok(const GemmArgs& a, cudaStream_t s) {
     switch (a.tok_tile) {
-        case 0: return run_gemm<MODE, 0>(a, s);
-        case 16: return run_gemm<MODE, 16>(a, s);
-        case 32: return run_gemm<MODE, 32>(a, s);
-        case 64: return run_gemm<MODE, 64>(a, s);
-        case 128: return run_gemm<MODE, 128>(a, s);
+        case 0: return run_gemm<MODE, 0, Q4>(a, s);
+        case 16: return run_gemm<MODE, 16, Q4>(a, s);
+        case 32: return run_gemm<MODE, 32, Q4>(a, s);
+        case 64: return run_gemm<MODE, 64, Q4>(a, s);
+        case 128: return run_gemm<MODE, 128, Q4>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -550,11 +688,19 @@ cudaError_t dispatch_tok(const GemmArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
+    if (a.w.bits == 4) {
+        if (a.ws.bits != 16 && a.has_shared) return cudaErrorInvalidValue;
+        switch (a.mode) {
+            case kGateUp: return dispatch_tok<kGateUp, true>(a, s);
+            case kDown: return dispatch_tok<kDown, true>(a, s);
+            default: return cudaErrorInvalidValue;  // the router is always bf16
+        }
+    }
     if (a.w.bits != 16) return cudaErrorInvalidValue;
     switch (a.mode) {
-        case kGateUp: return dispatch_tok<kGateUp>(a, s);
-        case kDown: return dispatch_tok<kDown>(a, s);
-        case kRouter: return dispatch_tok<kRouter>(a, s);
+        case kGateUp: return dispatch_tok<kGateUp, false>(a, s);
+        case kDown: return dispatch_tok<kDown, false>(a, s);
+        case kRouter: return dispatch_tok<kRouter, false>(a, s);
     }
     return cudaErrorInvalidValue;
 }

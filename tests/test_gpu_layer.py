@@ -143,6 +143,40 @@ def test_layer_empty_batch():
 
 
 # ------------------------------------------------------------------------------------
+# affine 4-bit experts (dequantised in the GEMM main loop); bar 3e-2 max, 1e-2 mean
+# ------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T", [64, 5, 33, 96, 300])
+def test_q4_layer_token_tiles(T):
+    w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=T, bits=4)
+    r = _check_forward(w, inputs.gen_layer(w, DEV, seed=20 + T))
+    print(T, r["max"], r["mean"])
+
+
+@pytest.mark.parametrize("T,d,I,E,K,G,tg", [
+    (300, 512, 384, 32, 4, 4, 2),
+    (700, 640, 128, 24, 6, 3, 2),
+])
+def test_q4_layer_multi_tile(T, d, I, E, K, G, tg):
+    w = inputs.Workload("mt4", T=T, d=d, E=E, I=I, top_k=K, n_group=G, topk_group=tg,
+                        norm_topk_prob=True, routed_scaling_factor=2.5, bias_var=0.05, bits=4)
+    _check_forward(w, inputs.gen_layer(w, DEV, seed=2))
+
+
+def test_q4_dequant_is_exact_for_integer_affine():
+    """scale = 1/64 and bias = -7.5/64: every dequantised weight (q - 7.5)/64 is exactly
+    representable in bf16, so the 4-bit path must meet the bf16 layer bar."""
+    w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=40, bits=4)
+    data = inputs.gen_layer(w, DEV, seed=5)
+    ex = data["experts"]
+    for k in ("gate", "up", "down"):
+        ex[k + "_s"].fill_(1.0 / 64)
+        ex[k + "_b"].fill_(-7.5 / 64)
+    r = _check_forward(w, data)
+    assert r["max"] < 1e-2 and r["mean"] < 5e-3
+
+
+# ------------------------------------------------------------------------------------
 # DeepSeek-V3-shaped layers at full size, outputs checked on sampled tokens
 # ------------------------------------------------------------------------------------
 
@@ -167,4 +201,28 @@ def test_dsv3_prefill_T8192_zipf(dsv3_weights):
     data["x"] = inputs.gen_tokens(w, DEV, seed=0)
     data["logit_offset"] = inputs.zipf_offsets(w.E, DEV, 0)
     r = _check_forward(w, data, rows=[0, 4095, 8191], check_logits_rows=np.arange(0, 8192, 97))
+    print(r["ties"], r["max"], r["mean"], int((r["counts"] > 0).sum()), int(r["counts"].max()))
+
+
+@pytest.fixture(scope="module")
+def dsv3_q4_weights():
+    w = inputs.WORKLOADS["dsv3_q4_T32"]
+    data = inputs.gen_layer(w, DEV, seed=0)
+    yield data
+    del data
+    torch.cuda.empty_cache()
+
+
+def test_dsv3_q4_decode_T32(dsv3_q4_weights):
+    w = inputs.WORKLOADS["dsv3_q4_T32"]
+    r = _check_forward(w, dsv3_q4_weights, rows=[0, 17, 31])
+    print(r["ties"], r["max"], r["mean"], int((r["counts"] > 0).sum()))
+
+
+def test_dsv3_q4_prefill_T4096_zipf(dsv3_q4_weights):
+    w = inputs.WORKLOADS["dsv3_q4_T4096_zipf"]
+    data = dict(dsv3_q4_weights)
+    data["x"] = inputs.gen_tokens(w, DEV, seed=0)
+    data["logit_offset"] = inputs.zipf_offsets(w.E, DEV, 0)
+    r = _check_forward(w, data, rows=[0, 2048, 4095], check_logits_rows=np.arange(0, 4096, 61))
     print(r["ties"], r["max"], r["mean"], int((r["counts"] > 0).sum()), int(r["counts"].max()))
