@@ -60,6 +60,21 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the phase
+// completes or `hint_ns` pass, issuing no instructions meanwhile (a plain spin would take
+// issue slots from the warps doing the work).
+MOE_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits until the phase with the given parity has completed.  Returns false (without
 // waiting further) once *abort is set by another role of the CTA (abort may be null: not
 // watched) or the wait exceeds `limit_ns`.
@@ -67,12 +82,10 @@ MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                        unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 63u) == 0u) {
-            if (abort && *abort) return false;
-            if (globaltimer() - t0 > limit_ns) return false;
-        }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;  // <= 0.2 ms per try
+        if (abort && *abort) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
 }
 
@@ -133,6 +146,16 @@ MOE_DEV void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Same with the A operand in TMEM (128 lanes = rows, 32-bit columns = 2 bf16 along K).
+MOE_DEV void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrives once on `bar` when every UMMA issued so far by this thread has completed.
 MOE_DEV void umma_commit(uint64_t* bar) {
     asm volatile(
@@ -183,6 +206,21 @@ MOE_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 MOE_DEV void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// registers -> TMEM: thread i of the warp writes N consecutive 32-bit columns of lane
+// (quarter*32 + i), starting at the column of taddr.
+MOE_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+MOE_DEV void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------------------------

@@ -67,18 +67,36 @@ struct Cfg {
     static constexpr int kFeat = kSwap ? 128 : (MODE == kGateUp ? 128 : 256);
     static constexpr int kXBytes = kTok * 128;
     static constexpr int kWBytes = kWRows * 128;
-    static constexpr int kRBytes = Q4 ? kWRows * 32 : 0;  // packed codes: 8 words per row
-    static constexpr int kStageBytes = kXBytes + kWBytes + kRBytes;
-    static constexpr int kThreadsCta = Q4 ? kThreads + 32 * kDequantWarps : kThreads;
-    static constexpr int kStages = cmin(12, (200 * 1024) / kStageBytes);
     static constexpr int kAccCols = kSwap ? kTok * kNW : 256;
-    static constexpr int kTmemCols = pow2ceil(cmax(32, 2 * kAccCols));
+    // 4-bit with tokens on N ("TMEM-A" path): the dequant warps write the bf16 weights
+    // straight into TMEM (tcgen05.st) and the UMMA reads its A operand from there, so the
+    // dequantised tile never crosses shared memory (which would otherwise carry 8x the HBM
+    // bytes: bf16 written, then read back by the tensor core).  An operand stage is then
+    // the token rows in shared memory plus kAStageCols TMEM columns of weights.
+    static constexpr bool kTA = Q4 && kSwap;
+    static constexpr int kAStageCols = kNW * 32;  // 64 bf16 of K = 32 columns per weight tile
+    static constexpr int kStageBytes = kTA ? kXBytes : kXBytes + kWBytes;  // smem per stage
+    // 4-bit: packed codes travel in a ring of their own.  A raw slot holds kRawKB k-blocks
+    // of every weight row of the tile (a 128-byte row segment, 128-byte swizzled), so each
+    // HBM access is as long as in the bf16 path and the dequant warps read it without bank
+    // conflicts.  On the TMEM-A path a raw slot also carries one k-block of the bf16 shared
+    // expert (the same bytes: 128-byte rows).
+    static constexpr int kRawKB = 4;
+    static constexpr int kRBytes = Q4 ? kWRows * 32 * kRawKB : 0;
+    static constexpr int kStages =
+        kTA ? cmin(8, (512 - 2 * kAccCols) / kAStageCols)
+            : cmin(12, (216 * 1024 - (Q4 ? 2 * kRBytes : 0)) / kStageBytes);
+    static constexpr int kRawStages =
+        !Q4 ? 0 : kTA ? cmin(8, (216 * 1024 - kStages * kStageBytes) / kRBytes) : 2;
+    static constexpr int kThreadsCta = Q4 ? kThreads + 32 + 32 * kDequantWarps : kThreads;
+    static constexpr int kTmemCols = kTA ? 512 : pow2ceil(cmax(32, 2 * kAccCols));
     static constexpr int kN = kSwap ? kTok : 256;
     static constexpr uint32_t kIdesc = idesc_bf16(128, kN);
     static constexpr int kMaxGroups = 1025;
-    // shared memory: stages | barriers | misc | tile prefix | row offsets
-    static constexpr int kBarOff = kStages * kStageBytes;
-    static constexpr int kNumBars = 3 * kStages + 5;
+    // shared memory: operand stages | raw stages | barriers | misc | tile prefix | row offsets
+    static constexpr int kRawOff = kStages * kStageBytes;
+    static constexpr int kBarOff = kRawOff + kRawStages * kRBytes;
+    static constexpr int kNumBars = 2 * kStages + 2 * kRawStages + 5;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kPrefixOff = kMiscOff + 16;
     static constexpr int kRowOffOff = kPrefixOff + 4 * (kMaxGroups + 1);
@@ -86,6 +104,9 @@ struct Cfg {
     static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert(kN % 16 == 0 && kN >= 16 && kN <= 256, "UMMA N for M = 128");
+    static_assert(!kTA || (kStages >= 2 && 2 * kAccCols + kStages * kAStageCols <= 512),
+                  "TMEM budget of the TMEM-A path");
+    static_assert(!Q4 || kRawStages >= 2, "raw ring depth");
 };
 
 struct KParams {
@@ -105,6 +126,7 @@ struct KParams {
     // 4-bit weights: fp16 scale / bias per group of 64 inputs, [rows_total, Kdim / 64]
     const unsigned short* qscale[2];
     const unsigned short* qbias[2];
+    int q_vec;  // 8 | Kdim/64 and 16-byte aligned scale/bias arrays: 16-byte group loads
 };
 
 // Eight packed 4-bit codes (element j in bits 4j..4j+3 of the word) -> eight bf16 weights
@@ -217,8 +239,9 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::kStages;
-    uint64_t* rawfull = bars + 2 * C::kStages;  // 4-bit: packed codes of the stage landed
-    uint64_t* tfull = bars + 3 * C::kStages;
+    uint64_t* rawfull = bars + 2 * C::kStages;            // 4-bit: codes of a raw slot landed
+    uint64_t* rawempty = rawfull + C::kRawStages;         // 4-bit: raw slot read, reusable
+    uint64_t* tfull = rawempty + C::kRawStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* done = tfull + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
@@ -235,7 +258,10 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], Q4 ? 1 + kDequantWarps : 1);
             mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < C::kRawStages; ++s) {
             mbar_init(&rawfull[s], 1);
+            mbar_init(&rawempty[s], kDequantWarps);
         }
         mbar_init(&tfull[0], 1);
         mbar_init(&tfull[1], 1);
@@ -299,19 +325,11 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
                     uint8_t* st = smem + s * C::kStageBytes;
                     const int kx = kb * kBK;
                     uint8_t* wst = st + C::kXBytes;
-                    if (Q4 && !ti.shared) {
-                        // token rows -> full[s]; packed codes -> rawfull[s] (the dequant
-                        // warps complete full[s] once the bf16 weights are in place)
+                    if (C::kTA || (Q4 && !ti.shared)) {
+                        // token rows only: the dequant warps fill the weight tile (TMEM on
+                        // the TMEM-A path, else shared memory) and complete full[s]
                         mbar_arrive_expect_tx(&full[s], C::kXBytes);
                         tma_load_2d(st, am, &full[s], kx, (int)ti.act_row, pol_x);
-                        uint8_t* rst = wst + C::kWBytes;
-                        mbar_arrive_expect_tx(&rawfull[s], C::kRBytes);
-                        if (MODE == kGateUp) {
-                            tma_load_2d(rst, w0, &rawfull[s], kb * 8, wrow, pol_w);
-                            tma_load_2d(rst + 128 * 32, w1, &rawfull[s], kb * 8, wrow, pol_w);
-                        } else {
-                            tma_load_2d(rst, w0, &rawfull[s], kb * 8, wrow, pol_w);
-                        }
                         continue;
                     }
                     mbar_arrive_expect_tx(&full[s], C::kXBytes + C::kWBytes);
@@ -322,16 +340,63 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
                     } else {
                         tma_load_2d(wst, w0, &full[s], kx, wrow, pol_w);
                     }
-                    if (Q4) mbar_arrive(&rawfull[s]);  // bf16 shared expert: nothing to dequantise
                 }
             }
             if (!ok) {
-                // let the copies already issued land before the CTA can exit
-                for (int n = (it > C::kStages ? it - C::kStages : 0); n < it; ++n) {
-                    const uint32_t par = (uint32_t)(n / C::kStages) & 1u;
-                    if (Q4) mbar_wait(&rawfull[n % C::kStages], par, nullptr, 100000000ull);
-                    mbar_wait(&full[n % C::kStages], par, nullptr, 100000000ull);
+                // let the copies already issued land before the CTA can exit (full[s] also
+                // waits for the dequant warps in the 4-bit case: bounded, then give up)
+                for (int n = (it > C::kStages ? it - C::kStages : 0); n < it; ++n)
+                    mbar_wait(&full[n % C::kStages], (uint32_t)(n / C::kStages) & 1u, nullptr,
+                              100000000ull);
+            }
+        }
+    } else if (Q4 && warp == kThreads / 32) {
+        // ======================= 4-bit: packed-code TMA producer =====================
+        // runs up to kRawStages k-blocks ahead of the dequant warps, independent of the
+        // operand ring, so enough HBM reads stay in flight to stream the codes at full rate
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            int rit = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
+                if (ti.shared) {
+                    // normal-mode 4-bit: the operand producer loads the bf16 shared rows;
+                    // TMEM-A path: one k-block of them per raw slot (same 128-byte rows)
+                    if (!C::kTA) continue;
+                    for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++rit) {
+                        const int rs = rit % C::kRawStages;
+                        const uint32_t rph = (uint32_t)(rit / C::kRawStages) & 1u;
+                        if (!mbar_wait(&rawempty[rs], rph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
+                        uint8_t* rst = smem + C::kRawOff + rs * C::kRBytes;
+                        mbar_arrive_expect_tx(&rawfull[rs], C::kRBytes);
+                        tma_load_2d(rst, &tm_sw0, &rawfull[rs], kb * kBK, ti.f * C::kFeat, pol_w);
+                        if (MODE == kGateUp)
+                            tma_load_2d(rst + 128 * 128, &tm_sw1, &rawfull[rs], kb * kBK,
+                                        ti.f * C::kFeat, pol_w);
+                    }
+                    continue;
                 }
+                const int wrow = ti.g * p.F + ti.f * C::kFeat;
+                for (int kb = ti.kb0; kb < ti.kb1; kb += C::kRawKB, ++rit) {
+                    const int rs = rit % C::kRawStages;
+                    const uint32_t rph = (uint32_t)(rit / C::kRawStages) & 1u;
+                    if (!mbar_wait(&rawempty[rs], rph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
+                    uint8_t* rst = smem + C::kRawOff + rs * C::kRBytes;
+                    mbar_arrive_expect_tx(&rawfull[rs], C::kRBytes);
+                    if (MODE == kGateUp) {
+                        tma_load_2d(rst, &tm_w0, &rawfull[rs], kb * 8, wrow, pol_w);
+                        tma_load_2d(rst + 128 * 32 * C::kRawKB, &tm_w1, &rawfull[rs], kb * 8, wrow,
+                                    pol_w);
+                    } else {
+                        tma_load_2d(rst, &tm_w0, &rawfull[rs], kb * 8, wrow, pol_w);
+                    }
+                }
+            }
+            if (!ok) {
+                for (int n = (rit > C::kRawStages ? rit - C::kRawStages : 0); n < rit; ++n)
+                    mbar_wait(&rawfull[n % C::kRawStages], (uint32_t)(n / C::kRawStages) & 1u,
+                              nullptr, 100000000ull);
             }
         }
     } else if (warp == 1) {
@@ -356,7 +421,16 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint32_t accum = (kb > ti.kb0 || kk > 0) ? 1u : 0u;
-                        if (C::kSwap) {
+                        if (C::kTA) {
+                            // A (weights) from this stage's TMEM columns, 8 per K=16 slice
+                            const uint64_t bd = sdesc_k128(xs + kk * 32);
+                            const uint32_t a0 = tmem_base + (uint32_t)(2 * C::kAccCols +
+                                                                       s * C::kAStageCols + kk * 8);
+#pragma unroll
+                            for (int w = 0; w < C::kNW; ++w)
+                                umma_bf16_ta(acc + (uint32_t)(w * C::kTok),
+                                             a0 + (uint32_t)(w * 32), bd, C::kIdesc, accum);
+                        } else if (C::kSwap) {
                             const uint64_t bd = sdesc_k128(xs + kk * 32);
 #pragma unroll
                             for (int w = 0; w < C::kNW; ++w)
@@ -383,52 +457,175 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
         // ============================ 4-bit dequantisation ==========================
         // 256 threads; thread dt owns row dt % kWRows of the stage's weight tile and
         // kWordsPT of its 8 packed words (one 64-element k-block = one scale group).
+        // On the TMEM-A path a warp may only write its own TMEM lane quarter, so the row
+        // follows the warp: quarter q = warp % 4, lane -> row q*32 + lane; the two warps of a
+        // quarter take the gate and the up tile (gate/up) or the two halves of a row (down).
         constexpr int kWordsPT = C::kWRows * 8 / (32 * kDequantWarps);
-        const int dt = threadIdx.x - kThreads;
-        const int r = dt % C::kWRows;
-        const int wd0 = (dt / C::kWRows) * kWordsPT;
+        const int dt = threadIdx.x - kThreads - 32;
+        const int qtr = warp & 3;
+        const int half = dt / (32 * kDequantWarps / 2);
+        const int r = C::kTA ? (MODE == kGateUp ? half * 128 : 0) + qtr * 32 + lane
+                             : dt % C::kWRows;
+        const int wd0 = C::kTA ? (MODE == kGateUp ? 0 : half * kWordsPT)
+                               : (dt / C::kWRows) * kWordsPT;
         const int mat = (MODE == kGateUp && r >= 128) ? 1 : 0;
         const int rr = (MODE == kGateUp) ? (r & 127) : r;
         const unsigned short* sp = mat ? p.qscale[1] : p.qscale[0];
         const unsigned short* bp = mat ? p.qbias[1] : p.qbias[0];
         const int kgroups = p.Kdim / kBK;
-        int it = 0;
+        // scale/bias of a row are contiguous over its groups: with 8 | kgroups (and 16-byte
+        // aligned arrays) they arrive 8 groups per 16-byte load, one chunk ahead of use;
+        // otherwise one group ahead.  Either way the global latency hides behind dequant work.
+        const bool vec = p.q_vec != 0;
+        int it = 0, rit = 0;  // operand-ring and raw-ring positions
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
             const bool rvalid = !ti.shared && ti.f * C::kFeat + rr < p.F;
             const long long grow = (long long)ti.g * p.F + ti.f * C::kFeat + rr;
+            const unsigned short* srow = sp + grow * kgroups;
+            const unsigned short* brow = bp + grow * kgroups;
+            uint4 sc_cur = make_uint4(0, 0, 0, 0), bc_cur = sc_cur, sc_nxt = sc_cur, bc_nxt = sc_cur;
+            unsigned short s_nxt = 0, b_nxt = 0;
+            if (rvalid) {
+                if (vec) {
+                    sc_cur = __ldg(reinterpret_cast<const uint4*>(srow + ti.kb0));
+                    bc_cur = __ldg(reinterpret_cast<const uint4*>(brow + ti.kb0));
+                    if (ti.kb0 + 8 < kgroups) {
+                        sc_nxt = __ldg(reinterpret_cast<const uint4*>(srow + ti.kb0 + 8));
+                        bc_nxt = __ldg(reinterpret_cast<const uint4*>(brow + ti.kb0 + 8));
+                    }
+                } else {
+                    s_nxt = __ldg(srow + ti.kb0);
+                    b_nxt = __ldg(brow + ti.kb0);
+                }
+            }
             for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++it) {
                 const int s = it % C::kStages;
                 const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
                 unsigned short sb = 0, bb = 0;  // fp16 bits of this row's scale and bias
-                if (rvalid) {
-                    sb = __ldg(sp + grow * kgroups + kb);
-                    bb = __ldg(bp + grow * kgroups + kb);
+                if (vec) {
+                    const int j = (kb - ti.kb0) & 7;
+                    if (j == 0 && kb > ti.kb0) {
+                        sc_cur = sc_nxt;
+                        bc_cur = bc_nxt;
+                        if (rvalid && kb + 8 < kgroups) {
+                            sc_nxt = __ldg(reinterpret_cast<const uint4*>(srow + kb + 8));
+                            bc_nxt = __ldg(reinterpret_cast<const uint4*>(brow + kb + 8));
+                        }
+                    }
+                    const uint32_t sw = j < 2 ? sc_cur.x : j < 4 ? sc_cur.y : j < 6 ? sc_cur.z : sc_cur.w;
+                    const uint32_t bw = j < 2 ? bc_cur.x : j < 4 ? bc_cur.y : j < 6 ? bc_cur.z : bc_cur.w;
+                    sb = (unsigned short)((j & 1) ? (sw >> 16) : (sw & 0xFFFFu));
+                    bb = (unsigned short)((j & 1) ? (bw >> 16) : (bw & 0xFFFFu));
+                } else {
+                    sb = s_nxt;
+                    bb = b_nxt;
+                    if (rvalid && kb + 1 < ti.kb1) {
+                        s_nxt = __ldg(srow + kb + 1);
+                        b_nxt = __ldg(brow + kb + 1);
+                    }
                 }
-                if (!mbar_wait(&rawfull[s], ph, abort)) { record_timeout(abort); ok = false; break; }
+                uint32_t words[kWordsPT];
+                if (!ti.shared) {
+                    // this row's codes of k-block kb from the current raw slot (a 128-byte
+                    // swizzled row segment of kRawKB k-blocks); the slot goes back to the
+                    // code producer after its last k-block
+                    const int j = (kb - ti.kb0) % C::kRawKB;
+                    const int rs = rit % C::kRawStages;
+                    if (j == 0) {
+                        const uint32_t rph = (uint32_t)(rit / C::kRawStages) & 1u;
+                        if (!mbar_wait(&rawfull[rs], rph, abort)) { record_timeout(abort); ok = false; break; }
+                    }
+                    const uint8_t* rrow = smem + C::kRawOff + rs * C::kRBytes + r * 128;
+#pragma unroll
+                    for (int v = 0; v < kWordsPT / 4; ++v) {
+                        const int c16 = 2 * j + (wd0 + 4 * v) / 4;  // 16-byte chunk in the row
+                        const uint4 q4 =
+                            *reinterpret_cast<const uint4*>(rrow + ((c16 ^ (r & 7)) << 4));
+                        words[4 * v] = q4.x; words[4 * v + 1] = q4.y;
+                        words[4 * v + 2] = q4.z; words[4 * v + 3] = q4.w;
+                    }
+                    if (j == C::kRawKB - 1 || kb + 1 == ti.kb1) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&rawempty[rs]);
+                        ++rit;
+                    }
+                } else if (C::kTA) {
+                    // bf16 shared expert on the TMEM-A path: one k-block per raw slot, the
+                    // row's 128 bytes are already the operand
+                    const int rs = rit % C::kRawStages;
+                    const uint32_t rph = (uint32_t)(rit / C::kRawStages) & 1u;
+                    if (!mbar_wait(&rawfull[rs], rph, abort)) { record_timeout(abort); ok = false; break; }
+                    const uint8_t* rrow = smem + C::kRawOff + rs * C::kRBytes + r * 128;
+                    uint4 bw[kWordsPT];
+#pragma unroll
+                    for (int w = 0; w < kWordsPT; ++w)
+                        bw[w] = *reinterpret_cast<const uint4*>(rrow + (((wd0 + w) ^ (r & 7)) << 4));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&rawempty[rs]);
+                    ++rit;
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t tcol = tmem_base + ((uint32_t)(qtr * 32) << 16) +
+                                          (uint32_t)(2 * C::kAccCols + s * C::kAStageCols +
+                                                     (MODE == kGateUp ? half * 32 : 0) + wd0 * 4);
+#pragma unroll
+                    for (int h = 0; h < kWordsPT / 4; ++h) {
+                        uint32_t v16[16];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            v16[4 * i] = bw[4 * h + i].x; v16[4 * i + 1] = bw[4 * h + i].y;
+                            v16[4 * i + 2] = bw[4 * h + i].z; v16[4 * i + 3] = bw[4 * h + i].w;
+                        }
+                        tmem_st16(tcol + (uint32_t)(16 * h), v16);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full[s]);
+                    continue;
+                }
+                // dequantise into registers first, so the math overlaps the wait for the
+                // operand slot (free once the MMA has consumed its previous contents)
+                uint4 dq8[kWordsPT];
                 if (!ti.shared) {
                     const float sf = __half2float(__ushort_as_half(sb));
                     const float bf = __half2float(__ushort_as_half(bb));
                     const uint32_t s2 = pack_bf16x2(sf, sf), b2 = pack_bf16x2(bf, bf);
-                    uint8_t* st = smem + s * C::kStageBytes;
-                    const uint8_t* rrow = st + C::kXBytes + C::kWBytes + r * 32;
-                    uint8_t* wrow_s = st + C::kXBytes + r * 128;
-                    uint32_t words[kWordsPT];
 #pragma unroll
-                    for (int v = 0; v < kWordsPT / 4; ++v) {
-                        const uint4 q4 = *reinterpret_cast<const uint4*>(rrow + (wd0 + 4 * v) * 4);
-                        words[4 * v] = q4.x; words[4 * v + 1] = q4.y;
-                        words[4 * v + 2] = q4.z; words[4 * v + 3] = q4.w;
-                    }
-#pragma unroll
-                    for (int w = 0; w < kWordsPT; ++w) {
-                        const int c = wd0 + w;  // 16-byte chunk = 8 elements of the row
-                        *reinterpret_cast<uint4*>(wrow_s + ((c ^ (r & 7)) << 4)) =
-                            dequant8(words[w], s2, b2);
-                    }
+                    for (int w = 0; w < kWordsPT; ++w) dq8[w] = dequant8(words[w], s2, b2);
                 }
-                fence_proxy_async_smem();
+                if (!mbar_wait(&empty[s], ph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
+                if (C::kTA) {
+                    // weights -> this stage's TMEM columns of the warp's lane quarter
+                    tc_fence_after();
+                    const uint32_t tcol = tmem_base + ((uint32_t)(qtr * 32) << 16) +
+                                          (uint32_t)(2 * C::kAccCols + s * C::kAStageCols +
+                                                     (MODE == kGateUp ? half * 32 : 0) + wd0 * 4);
+#pragma unroll
+                    for (int h = 0; h < kWordsPT / 4; ++h) {
+                        uint32_t v16[16];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            v16[4 * i] = dq8[4 * h + i].x; v16[4 * i + 1] = dq8[4 * h + i].y;
+                            v16[4 * i + 2] = dq8[4 * h + i].z; v16[4 * i + 3] = dq8[4 * h + i].w;
+                        }
+                        tmem_st16(tcol + (uint32_t)(16 * h), v16);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                } else {
+                    if (!ti.shared) {
+                        uint8_t* wrow_s = smem + s * C::kStageBytes + C::kXBytes + r * 128;
+#pragma unroll
+                        for (int w = 0; w < kWordsPT; ++w) {
+                            const int c = wd0 + w;  // 16-byte chunk = 8 elements of the row
+                            *reinterpret_cast<uint4*>(wrow_s + ((c ^ (r & 7)) << 4)) = dq8[w];
+                        }
+                    }
+                    fence_proxy_async_smem();
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[s]);
             }
@@ -595,8 +792,8 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D uint32 tensor [rows, cols_u32] of packed 4-bit codes, box of 8 words (64 codes) x
-// box_rows rows, no swizzle (the dequant warps read it row by row).
+// 2-D uint32 tensor [rows, cols_u32] of packed 4-bit codes, box of 32 words (4 groups of
+// 64 codes = one 128-byte row segment) x box_rows rows, 128-byte swizzle.
 bool make_map_q4(CUtensorMap* m, const void* base, long long rows, long long cols_u32,
                  int box_rows) {
     EncodeTiledFn enc = encode_fn();
@@ -604,10 +801,10 @@ bool make_map_q4(CUtensorMap* m, const void* base, long long rows, long long col
     if (rows < 1) rows = 1;
     const cuuint64_t dims[2] = {(cuuint64_t)cols_u32, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols_u32 * 4};
-    const cuuint32_t box[2] = {8u, (cuuint32_t)box_rows};
+    const cuuint32_t box[2] = {32u, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -664,6 +861,9 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
     p.qbias[0] = static_cast<const unsigned short*>(a.w.b0);
     p.qscale[1] = static_cast<const unsigned short*>(a.w.s1);
     p.qbias[1] = static_cast<const unsigned short*>(a.w.b1);
+    auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+    p.q_vec = Q4 && (a.Kdim / kBK) % 8 == 0 && a.ksplit == 1 && al16(a.w.s0) && al16(a.w.b0) &&
+              (MODE != kGateUp || (al16(a.w.s1) && al16(a.w.b1)));
 
     long long grid = num_sms();
     if (a.max_tiles < grid) grid = a.max_tiles;
@@ -680,7 +880,9 @@ cudaError_t dispatch_tok(const GemmArgs& a, cudaStream_t s) {
         case 16: return run_gemm<MODE, 16, Q4>(a, s);
         case 32: return run_gemm<MODE, 32, Q4>(a, s);
         case 64: return run_gemm<MODE, 64, Q4>(a, s);
-        case 128: return run_gemm<MODE, 128, Q4>(a, s);
+        case 128:  // the 4-bit TMEM-A path has no TMEM room for 128-token tiles
+            if constexpr (!Q4) return run_gemm<MODE, 128, Q4>(a, s);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
