@@ -125,13 +125,15 @@ int check_dims(int64_t T, int32_t d, int32_t I, int32_t E, int32_t K) {
     return MOE_OK;
 }
 
-// Token tile of the expert GEMMs: tokens on the N side (16..64) when the experts see few
-// tokens on average, else 128-token tiles on the M side.
-int expert_tok_tile(int64_t P, int32_t E) {
+// Token tile of the expert GEMMs.  With tokens on the N side an UMMA (M = 128 weight rows,
+// K = 16) costs the same for N = 16 .. 64 (its 128 x 16 A operand sets the pace), so wide
+// token tiles are free and avoid streaming a weight tile once per 16 tokens: 64-token tiles
+// while the experts see few tokens on average, 128 (bf16 only: the 4-bit TMEM-A path has no
+// TMEM room for them) for mid-size batches, else 128-token tiles on the M side.
+int expert_tok_tile(int64_t P, int32_t E, int32_t bits) {
     const int64_t avg = (P + E - 1) / E;
-    if (avg <= 12) return 16;
-    if (avg <= 24) return 32;
-    if (avg <= 48) return 64;
+    if (avg <= 40) return 64;
+    if (avg <= 96 && bits == 16) return 128;
     return 0;
 }
 
@@ -214,7 +216,7 @@ int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_
     const int has_shared = sh != nullptr;
     MOE_CUDA(moe::launch_gather_rows(x, perm, offsets, E, K, P, d, x_perm, s), "gather rows");
     MOE_CUDA(phase(4, s), "phase event");
-    const int tok = expert_tok_tile(P, E);
+    const int tok = expert_tok_tile(P, E, ex->bits);
     const int tokn = tok ? tok : 128;
     const long long mt_bound = (P + tokn - 1) / tokn + E + (has_shared ? (T + tokn - 1) / tokn : 0);
 
