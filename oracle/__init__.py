@@ -62,7 +62,9 @@ def _load():
             lib.oracle_dequant_q4.restype = None
             lib.oracle_moe_layer_rows.argtypes = (
                 [P, i64, i32, i32, i32, i32, P, P, i32, i32] + [P] * 9 + [i32] + [P] * 9
-                + [P, i64, P])
+                + [P, P, i64, P])
+            lib.oracle_route_softmax.argtypes = [P, i64, i32, i32, P, P]
+            lib.oracle_route_softmax.restype = ctypes.c_int
             lib.oracle_moe_layer_rows.restype = ctypes.c_int
             lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
             lib.oracle_bf16_to_f32.restype = f32
@@ -143,7 +145,22 @@ def dequant_q4(q, scale_f16_bits, bias_f16_bits, cols, group=64):
     return out
 
 
-def moe_layer(x_bits, inds, scores, experts, shared=None, rows=None, group=64):
+def route_softmax(logits, top_k):
+    """Softmax route on fp32 logits [..., E]: (inds int32, scores fp32) [..., K], weights
+    renormalised over the selected experts (always)."""
+    lib = _load()
+    lg = _c(logits, np.float32)
+    E = lg.shape[-1]
+    rows = lg.size // E if E else 0
+    inds = np.zeros(lg.shape[:-1] + (top_k,), np.int32)
+    scores = np.zeros(lg.shape[:-1] + (top_k,), np.float32)
+    if lib.oracle_route_softmax(_ptr(lg), rows, E, top_k, _ptr(inds), _ptr(scores)) != 0:
+        raise ValueError("oracle_route_softmax rejected its arguments")
+    return inds, scores
+
+
+def moe_layer(x_bits, inds, scores, experts, shared=None, rows=None, group=64,
+              shared_gate=None):
     """Dense per-token MoE layer; returns fp32 y for the listed token rows.
 
     x_bits: uint16 bf16 bits [T, d].  experts: dict with 'bits' (16 or 4) and, for 16,
@@ -172,13 +189,14 @@ def moe_layer(x_bits, inds, scores, experts, shared=None, rows=None, group=64):
     else:
         sg = su = sd = None
     rws = np.arange(T, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    sgv = None if shared_gate is None else _c(shared_gate, np.uint16)
     y = np.zeros((len(rws), d), np.float32)
     rc = lib.oracle_moe_layer_rows(
         _ptr(x), T, d, I, E, K, _ptr(ind), _ptr(sc), bits, group,
         _ptr(g), _ptr(gs), _ptr(gb), _ptr(u), _ptr(us), _ptr(ub), _ptr(dn), _ptr(ds), _ptr(db),
         1 if shared is not None else 0,
         _ptr(sg), None, None, _ptr(su), None, None, _ptr(sd), None, None,
-        _ptr(rws), len(rws), _ptr(y))
+        _ptr(sgv), _ptr(rws), len(rws), _ptr(y))
     if rc != 0:
         raise ValueError("oracle_moe_layer_rows: bad expert index or allocation failure")
     return y

@@ -177,6 +177,48 @@ int oracle_route(const float* logits, int64_t rows, int E, const float* bias, in
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* softmax route ([gate] "Scope decisions" and review "What looks solid" 1: the softmax */
+/* route of the generic MoE block always renormalises its top-k weights)                */
+/* ------------------------------------------------------------------------------------ */
+
+/* R19: softmax is strictly increasing in the logit, so the K most probable experts are the
+ * K largest logits (ties to the lower index, R1); the renormalised weight of a selected
+ * expert, p_k / sum_sel p_j, is exp(l_k - l_max) / sum_sel exp(l_j - l_max), which does not
+ * depend on the full softmax denominator.  fp32 throughout, sum left to right over k. */
+int oracle_route_softmax_row(const float* logits, int E, int top_k, int32_t* inds,
+                             float* scores) {
+    char* taken = (char*)calloc((size_t)E, 1);
+    if (!taken) return -1;
+    for (int k = 0; k < top_k; ++k) {
+        int best = -1;
+        for (int e = 0; e < E; ++e)
+            if (!taken[e] && (best < 0 || route_better(logits[e], e, logits[best], best))) best = e;
+        taken[best] = 1;
+        inds[k] = best;
+    }
+    float lmax = logits[inds[0]];
+    float sum = 0.0f;
+    for (int k = 0; k < top_k; ++k) {
+        scores[k] = expf(logits[inds[k]] - lmax);
+        sum += scores[k];
+    }
+    for (int k = 0; k < top_k; ++k) scores[k] = scores[k] / sum;
+    free(taken);
+    return 0;
+}
+
+int oracle_route_softmax(const float* logits, int64_t rows, int E, int top_k, int32_t* inds,
+                         float* scores) {
+    if (!logits || !inds || !scores || top_k < 1 || top_k > E) return -1;
+    int rc = 0;
+#pragma omp parallel for schedule(static) reduction(| : rc)
+    for (int64_t r = 0; r < rows; ++r)
+        rc |= oracle_route_softmax_row(logits + r * E, E, top_k, inds + r * top_k,
+                                       scores + r * top_k);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* token -> expert dispatch (R6)                                                        */
 /* ------------------------------------------------------------------------------------ */
 
@@ -301,7 +343,9 @@ static oracle_mat_t expert_slice(const oracle_mat_t* m, int64_t e, int64_t rows,
  * The layer as a dense per-token loop ([arch]):
  *   y[t] = sum_k scores[t, k] * FFN_{inds[t, k]}(x[t]) + FFN_shared(x[t]).
  * Experts are stacked: gate/up [E, I, d], down [E, d, I].  The shared expert (one FFN of
- * the same shape, always active, weight 1, no gate) is skipped when has_shared == 0.
+ * the same shape, always active, weight 1, no gate) is skipped when has_shared == 0; with
+ * shared_gate (bf16 [d]) non-NULL its output is scaled by sigmoid(x . shared_gate) instead
+ * (the gated shared expert of the combine's has_shared_expert_gate = true).
  * `rows` lists which tokens to evaluate (n_rows of them); y is [n_rows, d] fp32.
  */
 int oracle_moe_layer_rows(const uint16_t* x, int64_t T, int d, int I, int E, int K,
@@ -313,6 +357,7 @@ int oracle_moe_layer_rows(const uint16_t* x, int64_t T, int d, int I, int E, int
                           const void* sgate_w, const void* sgate_s, const void* sgate_b,
                           const void* sup_w, const void* sup_s, const void* sup_b,
                           const void* sdown_w, const void* sdown_s, const void* sdown_b,
+                          const void* shared_gate,
                           const int64_t* rows, int64_t n_rows, float* y) {
     (void)T;
     oracle_mat_t g = {bits, group, (const uint16_t*)gate_w, (const uint32_t*)gate_w,
@@ -342,7 +387,19 @@ int oracle_moe_layer_rows(const uint16_t* x, int64_t T, int d, int I, int E, int
             oracle_mat_t de = expert_slice(&dn, e, d, I);
             expert_ffn(v, d, I, &ge, &ue, &de, (double)scores[t * K + k], acc, h);
         }
-        if (has_shared) expert_ffn(v, d, I, &sg, &su, &sd, 1.0, acc, h);
+        if (has_shared) {
+            /* gated shared expert (the combine's has_shared_expert_gate): the shared output
+             * is scaled by sigmoid(x . w_gate_vec); weight 1 without a gate */
+            double gw = 1.0;
+            if (shared_gate) {
+                double z = 0.0;
+                for (int i = 0; i < d; ++i)
+                    z += (double)oracle_bf16_to_f32(v[i]) *
+                         (double)oracle_bf16_to_f32(((const uint16_t*)shared_gate)[i]);
+                gw = 1.0 / (1.0 + exp(-z));
+            }
+            expert_ffn(v, d, I, &sg, &su, &sd, gw, acc, h);
+        }
         for (int o = 0; o < d; ++o) y[ri * d + o] = (float)acc[o];
         free(acc);
         free(h);

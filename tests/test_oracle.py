@@ -477,3 +477,72 @@ def test_silu_sign_and_gate_up_roles():
                              np.ones((1, 1), np.float32), ex, None)
         assert abs(y[0, 3] - 0.5 * a / (1 + math.exp(-a)) * u) < 1e-6
         assert np.count_nonzero(y) == 1
+
+
+# ------------------------------------------------------------------------------------
+# softmax route and gated shared expert
+# ------------------------------------------------------------------------------------
+
+def test_softmax_route_matches_numpy_float64():
+    rng = np.random.RandomState(21)
+    for E, K in ((8, 1), (16, 4), (64, 6), (256, 8)):
+        lg = (rng.randn(40, E) * 2).astype(np.float32)
+        inds, w = oracle.route_softmax(lg, K)
+        l64 = lg.astype(np.float64)
+        p = np.exp(l64 - l64.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        ref_i = np.argsort(-p, axis=1, kind="stable")[:, :K]
+        assert np.array_equal(inds, ref_i)
+        ps = np.take_along_axis(p, ref_i, axis=1)
+        assert np.allclose(w, ps / ps.sum(1, keepdims=True), rtol=1e-6, atol=0)
+
+
+def test_softmax_route_ties_brute_force():
+    rng = np.random.RandomState(22)
+    for _ in range(30):
+        lg = rng.randint(-2, 3, size=10).astype(np.float32)
+        for K in (1, 2, 3, 5):
+            sel = _best_subset([float(v) for v in lg], K)
+            sel = sorted(sel, key=lambda e: (-float(lg[e]), e))
+            inds, w = oracle.route_softmax(lg[None], K)
+            assert inds[0].tolist() == sel
+            assert abs(float(w[0].astype(np.float64).sum()) - 1.0) < 1e-6
+
+
+def test_softmax_route_shift_invariant_and_k1():
+    rng = np.random.RandomState(23)
+    lg = rng.randn(20, 32).astype(np.float32)
+    i0, w0 = oracle.route_softmax(lg, 4)
+    i1, w1 = oracle.route_softmax(lg + np.float32(3.0), 4)
+    assert np.array_equal(i0, i1) and np.allclose(w0, w1, rtol=1e-5)
+    _, wk1 = oracle.route_softmax(lg, 1)
+    assert np.all(wk1 == 1.0)
+
+
+def test_gated_shared_expert_matches_numpy():
+    T, d, I, E, K = 4, 64, 64, 5, 2
+    x, ex, sh, inds, scores = _rand_layer(T, d, I, E, K, seed=31)
+    g = torch.Generator().manual_seed(32)
+    wsg = (torch.randn(d, generator=g) / 8).to(torch.bfloat16)
+    got = oracle.moe_layer(_bits(x), inds, scores, _to_oracle_experts(ex),
+                           {k: _bits(v) for k, v in sh.items()}, shared_gate=_bits(wsg))
+    xs = _f64(x)
+    ref = np.zeros((T, d))
+    for t in range(T):
+        for k in range(K):
+            ref[t] += scores[t, k] * _np_ffn(xs[t], *_np_expert_weights(ex, inds[t, k]))
+        gate = 1 / (1 + np.exp(-(xs[t] @ _f64(wsg))))
+        ref[t] += gate * _np_ffn(xs[t], _f64(sh["gate"]), _f64(sh["up"]), _f64(sh["down"]))
+    assert np.abs(got - ref).max() <= 1e-6 * np.abs(ref).max()
+
+
+def test_zero_shared_gate_halves_the_shared_expert():
+    T, d, I, E, K = 3, 64, 64, 4, 2
+    x, ex, sh, inds, scores = _rand_layer(T, d, I, E, K, seed=33)
+    oe = _to_oracle_experts(ex)
+    osh = {k: _bits(v) for k, v in sh.items()}
+    none = oracle.moe_layer(_bits(x), inds, scores, oe, None).astype(np.float64)
+    full = oracle.moe_layer(_bits(x), inds, scores, oe, osh).astype(np.float64)
+    half = oracle.moe_layer(_bits(x), inds, scores, oe, osh,
+                            shared_gate=np.zeros(d, np.uint16)).astype(np.float64)
+    assert np.allclose(half, none + 0.5 * (full - none), rtol=1e-5, atol=1e-6)
