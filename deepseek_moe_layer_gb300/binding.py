@@ -23,7 +23,10 @@ MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
 EXPORTS = ("moe_last_error", "moe_version", "moe_device_status", "moe_route_deepseek",
            "moe_permute", "moe_router_logits", "moe_grouped_swiglu",
            "moe_grouped_swiglu_workspace_bytes", "moe_combine", "moe_forward",
-           "moe_forward_workspace_bytes", "moe_set_phase_events", "moe_forward_noalloc")
+           "moe_forward_workspace_bytes", "moe_set_phase_events", "moe_forward_noalloc",
+           "moe_route_softmax", "moe_shared_gate", "moe_combine_gated", "moe_forward_ex",
+           "moe_forward_ex_workspace_bytes")
+MOE_ROUTE_DEEPSEEK, MOE_ROUTE_SOFTMAX = 0, 1
 
 
 class MoeError(RuntimeError):
@@ -44,6 +47,17 @@ class ExpertWeights(ctypes.Structure):
                 ("gate_scale", ctypes.c_void_p), ("gate_bias", ctypes.c_void_p),
                 ("up_scale", ctypes.c_void_p), ("up_bias", ctypes.c_void_p),
                 ("down_scale", ctypes.c_void_p), ("down_bias", ctypes.c_void_p)]
+
+
+class LayerArgs(ctypes.Structure):
+    _fields_ = [("route_kind", ctypes.c_int32), ("x", ctypes.c_void_p), ("T", ctypes.c_int64),
+                ("d", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("w_router", ctypes.c_void_p), ("logit_offset", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("params", RouteParams),
+                ("experts", ctypes.POINTER(ExpertWeights)),
+                ("shared", ctypes.POINTER(ExpertWeights)), ("w_shared_gate", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("inds_out", ctypes.c_void_p),
+                ("scores_out", ctypes.c_void_p), ("logits_out", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -83,9 +97,17 @@ def lib(path: str | None = None):
                                               ctypes.POINTER(RouteParams),
                                               ctypes.POINTER(ExpertWeights),
                                               ctypes.POINTER(ExpertWeights), P, P, P, P, P]
+            L.moe_route_softmax.argtypes = [P, ctypes.c_int, i64, i32, i32, P, P, P]
+            L.moe_shared_gate.argtypes = [P, i64, i32, P, P, P]
+            L.moe_combine_gated.argtypes = [P, P, P, P, P, i64, i32, i32, P, P]
+            L.moe_forward_ex.argtypes = [ctypes.POINTER(LayerArgs), P, sz, P]
+            L.moe_forward_ex_workspace_bytes.argtypes = [ctypes.POINTER(LayerArgs)]
+            L.moe_forward_ex_workspace_bytes.restype = sz
             for name in ("moe_device_status", "moe_route_deepseek", "moe_permute",
                          "moe_router_logits", "moe_grouped_swiglu", "moe_combine",
-                         "moe_forward", "moe_set_phase_events", "moe_forward_noalloc"):
+                         "moe_forward", "moe_set_phase_events", "moe_forward_noalloc",
+                         "moe_route_softmax", "moe_shared_gate", "moe_combine_gated",
+                         "moe_forward_ex"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -173,6 +195,49 @@ def route_deepseek(logits, bias, top_k, n_group, topk_group, norm_topk_prob,
     return inds, scores
 
 
+def route_softmax(logits, top_k, inds=None, scores=None, stream=None):
+    """Softmax route: logits [..., E] fp32/bf16 -> (inds int32, scores fp32) [..., K]."""
+    if logits.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("logits must be fp32 or bf16")
+    _need(logits, logits.dtype, "logits")
+    E = logits.shape[-1]
+    rows = logits.numel() // E if E else 0
+    shape = tuple(logits.shape[:-1]) + (int(top_k),)
+    if inds is None:
+        inds = torch.empty(shape, dtype=torch.int32, device=logits.device)
+    if scores is None:
+        scores = torch.empty(shape, dtype=torch.float32, device=logits.device)
+    dt = MOE_DTYPE_F32 if logits.dtype == torch.float32 else MOE_DTYPE_BF16
+    _check(lib().moe_route_softmax(_ptr(logits), dt, rows, E, int(top_k), _ptr(inds),
+                                   _ptr(scores), _stream(stream)))
+    return inds, scores
+
+
+def shared_gate(x, w_gate, stream=None):
+    """gate[t] = sigmoid(x[t] . w_gate): bf16 x [T, d], w_gate [d] -> fp32 [T]."""
+    _need(x, torch.bfloat16, "x")
+    _need(w_gate, torch.bfloat16, "w_gate", x.device)
+    T, d = x.shape
+    g = torch.empty(T, dtype=torch.float32, device=x.device)
+    _check(lib().moe_shared_gate(_ptr(x), T, d, _ptr(w_gate), _ptr(g), _stream(stream)))
+    return g
+
+
+def combine_gated(expert_out, scores, inv_perm, shared_out, gate, stream=None):
+    """y[t] = sum_k scores[t,k] expert_out[inv_perm[t*K+k]] + gate[t] shared_out[t]."""
+    _need(expert_out, torch.bfloat16, "expert_out")
+    _need(scores, torch.float32, "scores")
+    _need(inv_perm, torch.int32, "inv_perm")
+    _need(gate, torch.float32, "gate")
+    T, K = scores.shape
+    d = expert_out.shape[1]
+    y = torch.empty(T, d, dtype=torch.bfloat16, device=expert_out.device)
+    _check(lib().moe_combine_gated(_ptr(expert_out), _ptr(scores), _ptr(inv_perm),
+                                   _ptr(shared_out), _ptr(gate), T, K, d, _ptr(y),
+                                   _stream(stream)))
+    return y
+
+
 def permute(inds, E, stream=None):
     """inds int32 [T, K] -> (counts [E], offsets [E+1], perm [P], inv_perm [P]), int32."""
     _need(inds, torch.int32, "inds")
@@ -250,10 +315,17 @@ class MoELayer:
     """
 
     def __init__(self, w_router, bias, experts, shared, top_k, n_group, topk_group,
-                 norm_topk_prob, routed_scaling_factor, logit_offset=None):
+                 norm_topk_prob, routed_scaling_factor, logit_offset=None,
+                 route_kind=MOE_ROUTE_DEEPSEEK, w_shared_gate=None):
         _need(w_router, torch.bfloat16, "w_router")
         self.dev = w_router.device
-        _need(bias, torch.float32, "bias", self.dev)
+        if bias is not None:
+            _need(bias, torch.float32, "bias", self.dev)
+        if w_shared_gate is not None:
+            _need(w_shared_gate, torch.bfloat16, "w_shared_gate", self.dev)
+        self.route_kind, self.w_shared_gate = int(route_kind), w_shared_gate
+        # the DeepSeek body goes through moe_forward, anything else through moe_forward_ex
+        self.ex = self.route_kind != MOE_ROUTE_DEEPSEEK or w_shared_gate is not None
         self.w_router, self.bias, self.logit_offset = w_router, bias, logit_offset
         self.experts, self.shared = experts, shared
         self.E, self.d = w_router.shape
@@ -263,9 +335,34 @@ class MoELayer:
         self.ew, self.sw = expert_weights(experts), expert_weights(shared)
         self.ws = None
 
+    def _args(self, x, y, inds, scores, logits):
+        a = LayerArgs()
+        a.route_kind = self.route_kind
+        a.x, a.T, a.d, a.I, a.E = x.data_ptr(), x.shape[0], self.d, self.I, self.E
+        a.w_router = self.w_router.data_ptr()
+        a.logit_offset = None if self.logit_offset is None else self.logit_offset.data_ptr()
+        a.bias = None if self.bias is None else self.bias.data_ptr()
+        a.params = self.params
+        a.experts = ctypes.pointer(self.ew)
+        a.shared = ctypes.pointer(self.sw) if self.sw is not None else None
+        a.w_shared_gate = None if self.w_shared_gate is None else self.w_shared_gate.data_ptr()
+        a.y = None if y is None else y.data_ptr()
+        a.inds_out = None if inds is None else inds.data_ptr()
+        a.scores_out = None if scores is None else scores.data_ptr()
+        a.logits_out = None if logits is None else logits.data_ptr()
+        return a
+
     def workspace(self, T):
-        need = forward_workspace_bytes(T, self.d, self.I, self.E, self.params.top_k,
-                                       self.shared is not None)
+        if self.ex:
+            a = LayerArgs()
+            a.route_kind, a.T, a.d, a.I, a.E = self.route_kind, T, self.d, self.I, self.E
+            a.params = self.params
+            a.shared = ctypes.pointer(self.sw) if self.sw is not None else None
+            a.w_shared_gate = None if self.w_shared_gate is None else 1
+            need = lib().moe_forward_ex_workspace_bytes(ctypes.byref(a))
+        else:
+            need = forward_workspace_bytes(T, self.d, self.I, self.E, self.params.top_k,
+                                           self.shared is not None)
         if self.ws is None or self.ws.numel() < need:
             self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.dev)
         return self.ws
@@ -282,6 +379,10 @@ class MoELayer:
             inds = torch.empty(T, K, dtype=torch.int32, device=self.dev)
             scores = torch.empty(T, K, dtype=torch.float32, device=self.dev)
             logits = torch.empty(T, self.E, dtype=torch.float32, device=self.dev)
+        if self.ex:
+            a = self._args(x, y, inds, scores, logits)
+            _check(lib().moe_forward_ex(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)))
+            return (y, inds, scores, logits) if want_intermediates else y
         _check(lib().moe_forward(_ptr(x), T, d, self.I, self.E, _ptr(self.w_router),
                                  _ptr(self.bias), _ptr(self.logit_offset),
                                  ctypes.byref(self.params), ctypes.byref(self.ew), _ref(self.sw),

@@ -261,6 +261,138 @@ int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_
     return MOE_OK;
 }
 
+
+// Whole-layer workspace of moe_forward_ex: moe_forward's plus the per-token shared gate.
+struct ForwardExWs {
+    ForwardWs base;
+    size_t gate, total;
+};
+ForwardExWs forward_ex_ws(const moe_layer_args_t& a) {
+    ForwardExWs w;
+    w.base = forward_ws(a.T, a.d, a.I, a.E, a.params.top_k, a.shared != nullptr,
+                        router_ksplit_bound(a.d));
+    w.gate = w.base.total;
+    w.total = w.gate + (a.w_shared_gate ? align256((size_t)a.T * 4) : 0);
+    return w;
+}
+
+// The layer: router linear -> gate -> dispatch -> expert SwiGLU (+ shared) -> combine.
+int forward_impl(const moe_layer_args_t& A, void* ws, size_t ws_bytes, cudaStream_t s) {
+    const int64_t T = A.T;
+    const int32_t d = A.d, I = A.I, E = A.E;
+    const moe_route_params_t* params = &A.params;
+    const bool softmax = A.route_kind == MOE_ROUTE_SOFTMAX;
+    MOE_CHECK(A.route_kind == MOE_ROUTE_DEEPSEEK || softmax, "route_kind %d unknown",
+              (int)A.route_kind);
+    MOE_CHECK(A.w_router && (softmax || A.bias) && ws && (T == 0 || (A.x && A.y)),
+              "NULL pointer argument");
+    int rc;
+    if (softmax) {
+        MOE_CHECK(E >= 1 && E <= kMaxExperts, "E = %d outside [1, %d]", E, kMaxExperts);
+        MOE_CHECK(params->top_k >= 1 && params->top_k <= E, "top_k = %d outside [1, E = %d]",
+                  params->top_k, E);
+    } else {
+        rc = check_route_params(E, params);
+        if (rc) return rc;
+    }
+    const int32_t K = params->top_k;
+    rc = check_dims(T, d, I, E, K);
+    if (rc) return rc;
+    rc = check_weights(A.experts, "expert", 0);
+    if (rc) return rc;
+    if (A.shared) {
+        rc = check_weights(A.shared, "shared expert", 1);
+        if (rc) return rc;
+    }
+    MOE_CHECK(!A.w_shared_gate || A.shared, "w_shared_gate given without a shared expert");
+    MOE_CHECK(aligned(A.x, 16) && aligned(A.w_router, 16) && aligned(A.y, 16) &&
+                  aligned(A.w_shared_gate, 16),
+              "x, w_router, w_shared_gate and y must be 16-byte aligned");
+    MOE_CHECK(aligned(ws, 256), "ws must be 256-byte aligned");
+    const int has_shared = A.shared != nullptr;
+    const ForwardExWs lx = forward_ex_ws(A);
+    const ForwardWs& lw = lx.base;
+    MOE_CHECK(ws_bytes >= lx.total, "ws_bytes = %zu < %zu required", ws_bytes, lx.total);
+    if (T == 0) return MOE_OK;
+    rc = check_device();
+    if (rc) return rc;
+
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    const int64_t P = T * K;
+    float* lpart = reinterpret_cast<float*>(w + lw.logits_part);
+    int32_t* inds = A.inds_out ? A.inds_out : reinterpret_cast<int32_t*>(w + lw.inds);
+    float* scores = A.scores_out ? A.scores_out : reinterpret_cast<float*>(w + lw.scores);
+    int32_t* counts = reinterpret_cast<int32_t*>(w + lw.counts);
+    int32_t* offsets = reinterpret_cast<int32_t*>(w + lw.offsets);
+    int32_t* perm = reinterpret_cast<int32_t*>(w + lw.perm);
+    int32_t* inv = reinterpret_cast<int32_t*>(w + lw.inv);
+    void* eo = w + lw.expert_out;
+    float* sgate = A.w_shared_gate ? reinterpret_cast<float*>(w + lx.gate) : nullptr;
+
+    MOE_CUDA(phase(0, s), "phase event");
+    // a1: router linear, K-split partial sums
+    const RouterPlan rp = router_plan(T, d, E);
+    moe::GemmArgs g = {};
+    g.mode = moe::kRouter;
+    g.act = A.x;
+    g.act_rows = T;
+    g.offsets = nullptr;
+    g.single_rows = T;
+    g.E = 1;
+    g.Kdim = d;
+    g.F = E;
+    g.ksplit = rp.ksplit;
+    g.split_stride = (long long)T * E;
+    g.w = {16, A.w_router, nullptr, nullptr, nullptr, nullptr, nullptr};
+    g.out = lpart;
+    g.out_ld = E;
+    g.tok_tile = rp.tok_tile;
+    g.max_tiles = rp.tiles;
+    MOE_CUDA(moe::launch_gemm(g, s), "router GEMM");
+    MOE_CUDA(phase(1, s), "phase event");
+
+    // a2: gate (sums the partials in split order, adds the offset)
+    moe::RouteArgs ra = {};
+    ra.logits = lpart;
+    ra.bf16 = 0;
+    ra.nsplit = rp.ksplit;
+    ra.split_stride = (long long)T * E;
+    ra.logit_offset = A.logit_offset;
+    ra.bias = A.bias;
+    ra.rows = T;
+    ra.E = E;
+    ra.top_k = K;
+    ra.n_group = softmax ? 1 : params->n_group;
+    ra.topk_group = softmax ? 1 : params->topk_group;
+    ra.norm = params->norm_topk_prob != 0;
+    ra.scale = params->routed_scaling_factor;
+    ra.inds = inds;
+    ra.scores = scores;
+    ra.logits_out = A.logits_out;
+    ra.softmax = softmax ? 1 : 0;
+    MOE_CUDA(moe::launch_route(ra, s), "route kernel");
+    MOE_CUDA(phase(2, s), "phase event");
+
+    // a3: dispatch
+    MOE_CUDA(moe::launch_permute(inds, P, E, counts, offsets, perm, inv, s), "permute kernel");
+    MOE_CUDA(phase(3, s), "phase event");
+
+    // a4 + a5 (+ a7): expert SwiGLU GEMMs, shared expert as the last group
+    rc = run_swiglu(A.x, T, d, I, E, K, offsets, perm, A.experts, A.shared, eo, w + lw.swiglu,
+                    s);
+    if (rc) return rc;
+
+    // a6: combine (the gated shared expert weighs its row by sigmoid(x . w_shared_gate))
+    if (sgate)
+        MOE_CUDA(moe::launch_shared_gate(A.x, T, d, A.w_shared_gate, sgate, s), "shared gate");
+    const void* so = has_shared ? static_cast<const void*>(static_cast<const uint8_t*>(eo) +
+                                                           (size_t)P * d * 2)
+                                : nullptr;
+    MOE_CUDA(moe::launch_combine(eo, scores, inv, so, T, K, d, A.y, s, sgate), "combine kernel");
+    MOE_CUDA(phase(7, s), "phase event");
+    return MOE_OK;
+}
+
 }  // namespace
 
 int moe::set_error(int code, const char* msg) {
@@ -434,97 +566,99 @@ int moe_forward(const void* x, int64_t T, int32_t d, int32_t I, int32_t E,
                 float* scores_out, float* logits_out, void* ws, size_t ws_bytes,
                 moe_stream_t stream) {
     g_err.clear();
-    MOE_CHECK(w_router && bias && ws && (T == 0 || (x && y)), "NULL pointer argument");
-    int rc = check_route_params(E, params);
+    MOE_CHECK(params, "params is NULL");
+    moe_layer_args_t a = {};
+    a.route_kind = MOE_ROUTE_DEEPSEEK;
+    a.x = x;
+    a.T = T;
+    a.d = d;
+    a.I = I;
+    a.E = E;
+    a.w_router = w_router;
+    a.logit_offset = logit_offset;
+    a.bias = bias;
+    a.params = *params;
+    a.experts = experts;
+    a.shared = shared;
+    a.w_shared_gate = nullptr;
+    a.y = y;
+    a.inds_out = inds_out;
+    a.scores_out = scores_out;
+    a.logits_out = logits_out;
+    return forward_impl(a, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+size_t moe_forward_ex_workspace_bytes(const moe_layer_args_t* a) {
+    if (!a || a->T < 0 || a->d < 0 || a->I < 0 || a->E < 0 || a->params.top_k < 0) return 0;
+    return forward_ex_ws(*a).total;
+}
+
+int moe_forward_ex(const moe_layer_args_t* args, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(args, "args is NULL");
+    return forward_impl(*args, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int moe_route_softmax(const void* logits, moe_dtype_t dtype, int64_t rows, int32_t E,
+                      int32_t top_k, int32_t* inds, float* scores, moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(rows == 0 || (logits && inds && scores), "NULL pointer argument");
+    MOE_CHECK(dtype == MOE_DTYPE_F32 || dtype == MOE_DTYPE_BF16, "dtype %d unknown", (int)dtype);
+    MOE_CHECK(rows >= 0, "rows = %lld < 0", (long long)rows);
+    MOE_CHECK(E >= 1 && E <= kMaxExperts, "E = %d outside [1, %d]", E, kMaxExperts);
+    MOE_CHECK(top_k >= 1 && top_k <= E && top_k <= kMaxTopK, "top_k = %d outside [1, min(E, %d)]",
+              top_k, kMaxTopK);
+    if (rows == 0) return MOE_OK;
+    int rc = check_device();
     if (rc) return rc;
-    const int32_t K = params->top_k;
-    rc = check_dims(T, d, I, E, K);
-    if (rc) return rc;
-    rc = check_weights(experts, "expert", 0);
-    if (rc) return rc;
-    if (shared) {
-        rc = check_weights(shared, "shared expert", 1);
-        if (rc) return rc;
-    }
-    MOE_CHECK(aligned(x, 16) && aligned(w_router, 16) && aligned(y, 16),
-              "x, w_router and y must be 16-byte aligned");
-    MOE_CHECK(aligned(ws, 256), "ws must be 256-byte aligned");
-    const int has_shared = shared != nullptr;
-    const ForwardWs lw = forward_ws(T, d, I, E, K, has_shared, router_ksplit_bound(d));
-    MOE_CHECK(ws_bytes >= lw.total, "ws_bytes = %zu < %zu required", ws_bytes, lw.total);
+    moe::RouteArgs a = {};
+    a.logits = logits;
+    a.bf16 = dtype == MOE_DTYPE_BF16;
+    a.nsplit = 1;
+    a.rows = rows;
+    a.E = E;
+    a.top_k = top_k;
+    a.n_group = 1;
+    a.topk_group = 1;
+    a.scale = 1.0f;
+    a.inds = inds;
+    a.scores = scores;
+    a.softmax = 1;
+    MOE_CUDA(moe::launch_route(a, (cudaStream_t)stream), "route kernel");
+    return MOE_OK;
+}
+
+int moe_shared_gate(const void* x, int64_t T, int32_t d, const void* w_gate, float* gate,
+                    moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(w_gate && (T == 0 || (x && gate)), "NULL pointer argument");
+    MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
+    MOE_CHECK(d >= 8 && d % 8 == 0, "d = %d must be a positive multiple of 8", d);
+    MOE_CHECK(aligned(x, 16) && aligned(w_gate, 16), "x and w_gate must be 16-byte aligned");
     if (T == 0) return MOE_OK;
-    rc = check_device();
+    int rc = check_device();
     if (rc) return rc;
+    MOE_CUDA(moe::launch_shared_gate(x, T, d, w_gate, gate, (cudaStream_t)stream), "shared gate");
+    return MOE_OK;
+}
 
-    cudaStream_t s = (cudaStream_t)stream;
-    uint8_t* w = static_cast<uint8_t*>(ws);
-    const int64_t P = T * K;
-    float* lpart = reinterpret_cast<float*>(w + lw.logits_part);
-    int32_t* inds = inds_out ? inds_out : reinterpret_cast<int32_t*>(w + lw.inds);
-    float* scores = scores_out ? scores_out : reinterpret_cast<float*>(w + lw.scores);
-    int32_t* counts = reinterpret_cast<int32_t*>(w + lw.counts);
-    int32_t* offsets = reinterpret_cast<int32_t*>(w + lw.offsets);
-    int32_t* perm = reinterpret_cast<int32_t*>(w + lw.perm);
-    int32_t* inv = reinterpret_cast<int32_t*>(w + lw.inv);
-    void* eo = w + lw.expert_out;
-
-    MOE_CUDA(phase(0, s), "phase event");
-    // a1: router linear, K-split partial sums
-    const RouterPlan rp = router_plan(T, d, E);
-    moe::GemmArgs g = {};
-    g.mode = moe::kRouter;
-    g.act = x;
-    g.act_rows = T;
-    g.offsets = nullptr;
-    g.single_rows = T;
-    g.E = 1;
-    g.Kdim = d;
-    g.F = E;
-    g.ksplit = rp.ksplit;
-    g.split_stride = (long long)T * E;
-    g.w = {16, w_router, nullptr, nullptr, nullptr, nullptr, nullptr};
-    g.out = lpart;
-    g.out_ld = E;
-    g.tok_tile = rp.tok_tile;
-    g.max_tiles = rp.tiles;
-    MOE_CUDA(moe::launch_gemm(g, s), "router GEMM");
-    MOE_CUDA(phase(1, s), "phase event");
-
-    // a2: gate (sums the partials in split order, adds the offset)
-    moe::RouteArgs ra = {};
-    ra.logits = lpart;
-    ra.bf16 = 0;
-    ra.nsplit = rp.ksplit;
-    ra.split_stride = (long long)T * E;
-    ra.logit_offset = logit_offset;
-    ra.bias = bias;
-    ra.rows = T;
-    ra.E = E;
-    ra.top_k = K;
-    ra.n_group = params->n_group;
-    ra.topk_group = params->topk_group;
-    ra.norm = params->norm_topk_prob != 0;
-    ra.scale = params->routed_scaling_factor;
-    ra.inds = inds;
-    ra.scores = scores;
-    ra.logits_out = logits_out;
-    MOE_CUDA(moe::launch_route(ra, s), "route kernel");
-    MOE_CUDA(phase(2, s), "phase event");
-
-    // a3: dispatch
-    MOE_CUDA(moe::launch_permute(inds, P, E, counts, offsets, perm, inv, s), "permute kernel");
-    MOE_CUDA(phase(3, s), "phase event");
-
-    // a4 + a5 (+ a7): expert SwiGLU GEMMs, shared expert as the last group
-    rc = run_swiglu(x, T, d, I, E, K, offsets, perm, experts, shared, eo, w + lw.swiglu, s);
+int moe_combine_gated(const void* expert_out, const float* scores, const int32_t* inv_perm,
+                      const void* shared_out, const float* shared_gate, int64_t T, int32_t K,
+                      int32_t d, void* y, moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(T == 0 || (expert_out && scores && inv_perm && shared_out && shared_gate && y),
+              "NULL pointer argument");
+    MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
+    MOE_CHECK(K >= 1, "K = %d < 1", K);
+    MOE_CHECK(d >= 8 && d % 8 == 0, "d = %d must be a positive multiple of 8", d);
+    MOE_CHECK(aligned(expert_out, 16) && aligned(y, 16) && aligned(shared_out, 16),
+              "expert_out, shared_out and y must be 16-byte aligned");
+    if (T == 0) return MOE_OK;
+    int rc = check_device();
     if (rc) return rc;
-
-    // a6: combine
-    const void* so = has_shared ? static_cast<const void*>(static_cast<const uint8_t*>(eo) +
-                                                           (size_t)P * d * 2)
-                                : nullptr;
-    MOE_CUDA(moe::launch_combine(eo, scores, inv, so, T, K, d, y, s), "combine kernel");
-    MOE_CUDA(phase(7, s), "phase event");
+    MOE_CUDA(moe::launch_combine(expert_out, scores, inv_perm, shared_out, T, K, d, y,
+                                 (cudaStream_t)stream, shared_gate),
+             "combine kernel");
     return MOE_OK;
 }
 

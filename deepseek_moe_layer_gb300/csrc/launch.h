@@ -23,6 +23,7 @@ struct RouteArgs {
     int32_t* inds;               // [rows, K]
     float* scores;               // [rows, K]
     float* logits_out;           // [rows, E] copy of the summed logits, or nullptr
+    int softmax;                 // 1: softmax route (bias, groups, norm, scale unused)
 };
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 // logits[t, e] += offset[e] for a [T, E] fp32 matrix.
@@ -37,9 +38,13 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t
                                int K, long long P, int d, void* x_perm, cudaStream_t s);
 
 // ---- combine ------------------------------------------------------------------------
+// shared_gate: [T] per-token weight of the shared expert's row, or nullptr for weight 1.
 cudaError_t launch_combine(const void* expert_out, const float* scores, const int32_t* inv,
                            const void* shared_out, long long T, int K, int d, void* y,
-                           cudaStream_t s);
+                           cudaStream_t s, const float* shared_gate = nullptr);
+// gate[t] = sigmoid(x[t] . w) for bf16 x [T, d] and w [d].
+cudaError_t launch_shared_gate(const void* x, long long T, int d, const void* w, float* gate,
+                               cudaStream_t s);
 
 // ---- expert GEMMs (tcgen05) ---------------------------------------------------------
 enum GemmMode { kGateUp = 0, kDown = 1, kRouter = 2 };

@@ -1,4 +1,4 @@
-// route.cu -- the DeepSeek gate, one warp per token.
+// route.cu -- the DeepSeek gate (and the softmax route), one warp per token.
 //
 // Source: "feat(engine): E1 DeepSeek-style MoE gate (sigmoid, group top-k, bias) (#108)",
 // section "Algorithm (mlx-lm group_expert_select)": sigmoid of the f32 logits, bias added
@@ -30,7 +30,11 @@ MOE_DEV float okey_value(uint32_t k) {
     return __uint_as_float(u);
 }
 
-template <int EPL>
+// SOFTMAX: the softmax route instead of the DeepSeek gate: the K largest logits are
+// selected (softmax is strictly increasing, so they are the K most probable experts) and
+// their weights exp(l_k - l_max) / sum_sel exp(l_j - l_max) are the selected softmax
+// probabilities renormalised over the selection, always (no bias, groups or scale).
+template <int EPL, bool SOFTMAX>
 __global__ void __launch_bounds__(256) route_kernel(const RouteArgs a) {
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -110,9 +114,14 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteArgs a) {
             float l = lg[i];
             if (a.logit_offset) l = l + a.logit_offset[e];
             if (a.logits_out) a.logits_out[row * E + e] = l;
-            const float s = 1.0f / (1.0f + expf(-l));
-            orig[i] = s;
-            key[i] = okey(s + a.bias[e]);
+            if (SOFTMAX) {
+                orig[i] = l;  // the logit itself is carried to the weights
+                key[i] = okey(l);
+            } else {
+                const float s = 1.0f / (1.0f + expf(-l));
+                orig[i] = s;
+                key[i] = okey(s + a.bias[e]);
+            }
         } else {
             orig[i] = 0.0f;
             key[i] = 0u;
@@ -122,7 +131,7 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteArgs a) {
 
     // ---- group mask: keep the topk_group groups with the largest top-2 sums ----
     const int G = a.n_group;
-    if (G > 1 && G - a.topk_group > 0) {
+    if (!SOFTMAX && G > 1 && G - a.topk_group > 0) {
         const int eg = E / G;
         uint32_t my_gk = 0;  // lane g (< G) holds the key of group g's score
         const int lpg = (eg % EPL == 0) ? eg / EPL : 0;
@@ -206,6 +215,18 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteArgs a) {
         if (lane == r) { my_w = ov; my_idx = (int)w; }
     }
 
+    if (SOFTMAX) {
+        // exp relative to the largest selected logit, renormalised over the selection
+        const float lmax = __shfl_sync(kFull, my_w, 0);
+        const float ex = lane < K ? expf(my_w - lmax) : 0.0f;
+        float sum = 0.0f;
+        for (int k = 0; k < K; ++k) sum += __shfl_sync(kFull, ex, k);
+        if (lane < K) {
+            a.inds[row * K + lane] = my_idx;
+            a.scores[row * K + lane] = ex / sum;
+        }
+        return;
+    }
     // ---- weights: renormalise (K > 1 and norm), then scale ----
     if (K > 1 && a.norm) {
         float sum = 0.0f;
@@ -240,13 +261,24 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     const unsigned grid = (unsigned)((a.rows + 7) / 8);
     const int epl = a.E <= 32 ? 1 : a.E <= 64 ? 2 : a.E <= 128 ? 4 : a.E <= 256 ? 8
                   : a.E <= 512 ? 16 : 32;
+    if (a.softmax) {
+        switch (epl) {
+            case 1: route_kernel<1, true><<<grid, 256, 0, s>>>(a); break;
+            case 2: route_kernel<2, true><<<grid, 256, 0, s>>>(a); break;
+            case 4: route_kernel<4, true><<<grid, 256, 0, s>>>(a); break;
+            case 8: route_kernel<8, true><<<grid, 256, 0, s>>>(a); break;
+            case 16: route_kernel<16, true><<<grid, 256, 0, s>>>(a); break;
+            default: route_kernel<32, true><<<grid, 256, 0, s>>>(a); break;
+        }
+        return cudaGetLastError();
+    }
     switch (epl) {
-        case 1: route_kernel<1><<<grid, 256, 0, s>>>(a); break;
-        case 2: route_kernel<2><<<grid, 256, 0, s>>>(a); break;
-        case 4: route_kernel<4><<<grid, 256, 0, s>>>(a); break;
-        case 8: route_kernel<8><<<grid, 256, 0, s>>>(a); break;
-        case 16: route_kernel<16><<<grid, 256, 0, s>>>(a); break;
-        default: route_kernel<32><<<grid, 256, 0, s>>>(a); break;
+        case 1: route_kernel<1, false><<<grid, 256, 0, s>>>(a); break;
+        case 2: route_kernel<2, false><<<grid, 256, 0, s>>>(a); break;
+        case 4: route_kernel<4, false><<<grid, 256, 0, s>>>(a); break;
+        case 8: route_kernel<8, false><<<grid, 256, 0, s>>>(a); break;
+        case 16: route_kernel<16, false><<<grid, 256, 0, s>>>(a); break;
+        default: route_kernel<32, false><<<grid, 256, 0, s>>>(a); break;
     }
     return cudaGetLastError();
 }

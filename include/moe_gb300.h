@@ -115,6 +115,19 @@ int moe_route_deepseek(const void* logits, moe_dtype_t dtype, int64_t rows, int3
                        float* scores, moe_stream_t stream);
 
 /*
+ * moe_route_softmax -- the softmax route of the generic MoE block ([gate] "Scope decisions"
+ * and review "What looks solid" 1: the softmax route always renormalises its top-k, unlike
+ * the DeepSeek gate).  logits [rows, E] fp32 or bf16.  Out: inds [rows, K] (the K largest
+ * logits = the K most probable experts; descending, ties to the lower index), scores
+ * [rows, K] = the selected softmax probabilities renormalised over the selection, computed
+ * as exp(l_k - l_max) / sum_sel exp(l_j - l_max) in fp32 (K = 1 gives 1.0).
+ * Errors: MOE_ERR_INVALID for NULL pointers, rows < 0, E < 1 or > 1024, top_k outside
+ * [1, min(E, 32)], an unknown dtype.  rows == 0 is a no-op.
+ */
+int moe_route_softmax(const void* logits, moe_dtype_t dtype, int64_t rows, int32_t E,
+                      int32_t top_k, int32_t* inds, float* scores, moe_stream_t stream);
+
+/*
  * moe_permute -- token-to-expert dispatch ([epic] first paragraph: the grouping that
  * gather_mm / gather_qmm consume).  inds [T, K] int32 expert ids of the P = T*K pairs
  * p = t*K + k.
@@ -176,6 +189,25 @@ int moe_combine(const void* expert_out, const float* scores, const int32_t* inv_
                 moe_stream_t stream);
 
 /*
+ * moe_shared_gate -- per-token weight of a gated shared expert ([gate] "Architecture and
+ * design": the combine's has_shared_expert_gate option): gate[t] = sigmoid(x[t] . w_gate),
+ * bf16 x [T, d] and w_gate [d], fp32 products and sum.  Out: gate fp32 [T].
+ * Errors: MOE_ERR_INVALID for NULL pointers, T < 0, d % 8 != 0, misaligned x / w_gate.
+ */
+int moe_shared_gate(const void* x, int64_t T, int32_t d, const void* w_gate, float* gate,
+                    moe_stream_t stream);
+
+/*
+ * moe_combine_gated -- moe_combine with the gated shared expert:
+ *     y[t] = sum_k scores[t,k] * expert_out[inv_perm[t*K+k]] + shared_gate[t] * shared_out[t]
+ * shared_gate fp32 [T] (e.g. from moe_shared_gate).  Other arguments and errors as
+ * moe_combine; shared_out and shared_gate are required.
+ */
+int moe_combine_gated(const void* expert_out, const float* scores, const int32_t* inv_perm,
+                      const void* shared_out, const float* shared_gate, int64_t T, int32_t K,
+                      int32_t d, void* y, moe_stream_t stream);
+
+/*
  * moe_forward -- the whole layer: router linear, gate, dispatch, expert SwiGLU (+ shared
  * expert), combine.  Arguments as in the calls above; y bf16 [T, d].  inds_out [T, K],
  * scores_out [T, K] and logits_out [T, E] are optional copies of the intermediate results
@@ -191,6 +223,42 @@ int moe_forward(const void* x, int64_t T, int32_t d, int32_t I, int32_t E,
 
 size_t moe_forward_workspace_bytes(int64_t T, int32_t d, int32_t I, int32_t E, int32_t top_k,
                                    int32_t has_shared);
+
+/*
+ * moe_forward_ex -- the layer with a choice of gate and an optional shared-expert gate:
+ * route_kind MOE_ROUTE_DEEPSEEK (moe_route_deepseek; bias required) or MOE_ROUTE_SOFTMAX
+ * (moe_route_softmax; bias, groups, norm and scale unused), and w_shared_gate bf16 [d]
+ * (non-NULL: the shared expert's output is weighted by sigmoid(x . w_shared_gate), as in
+ * moe_combine_gated; NULL: weight 1).  Every other field as in moe_forward.
+ * ws: at least moe_forward_ex_workspace_bytes(args) bytes, 256-byte aligned.
+ * Errors: those of moe_forward, an unknown route_kind, w_shared_gate without a shared
+ * expert.
+ */
+typedef enum { MOE_ROUTE_DEEPSEEK = 0, MOE_ROUTE_SOFTMAX = 1 } moe_route_kind_t;
+
+typedef struct {
+    int32_t route_kind;
+    const void* x;
+    int64_t T;
+    int32_t d;
+    int32_t I;
+    int32_t E;
+    const void* w_router;
+    const float* logit_offset;
+    const float* bias;
+    moe_route_params_t params;
+    const moe_expert_weights_t* experts;
+    const moe_expert_weights_t* shared;
+    const void* w_shared_gate;
+    void* y;
+    int32_t* inds_out;
+    float* scores_out;
+    float* logits_out;
+} moe_layer_args_t;
+
+int moe_forward_ex(const moe_layer_args_t* args, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+size_t moe_forward_ex_workspace_bytes(const moe_layer_args_t* args);
 
 /*
  * moe_forward_noalloc -- moe_forward without a caller workspace.  The pages have no

@@ -133,6 +133,99 @@ def test_parts_router_swiglu_combine():
     check_layer(y.float().cpu().numpy(), ref)
 
 
+# ------------------------------------------------------------------------------------
+# moe_forward_ex: softmax route and the sigmoid-gated shared expert
+# ------------------------------------------------------------------------------------
+
+def _check_forward_ex(w, data, route_kind, wsg):
+    layer = binding.MoELayer(data["w_router"],
+                             data["bias"] if route_kind == binding.MOE_ROUTE_DEEPSEEK else None,
+                             data["experts"], data["shared"], w.top_k, w.n_group, w.topk_group,
+                             w.norm_topk_prob, w.routed_scaling_factor, data["logit_offset"],
+                             route_kind=route_kind, w_shared_gate=wsg)
+    y, inds, scores, logits = layer(data["x"], want_intermediates=True)
+    torch.cuda.synchronize()
+    binding.device_status()
+    lg = logits.cpu().numpy()
+    xb = bits(data["x"])
+    off = None if data["logit_offset"] is None else data["logit_offset"].cpu().numpy()
+    ref_lg = oracle.router_logits(xb, bits(data["w_router"]), off)
+    assert np.abs(lg - ref_lg).max() <= 1e-5 * np.abs(ref_lg).max()
+    rows = np.arange(w.T)
+    if route_kind == binding.MOE_ROUTE_SOFTMAX:
+        ri, rs = oracle.route_softmax(lg, w.top_k)
+        assert np.array_equal(inds.cpu().numpy(), ri)
+        np.testing.assert_allclose(scores.cpu().numpy(), rs, rtol=2e-6, atol=1e-12)
+    else:
+        bias = data["bias"].cpu().numpy()
+        ri, rs = oracle.route(lg, bias, w.top_k, w.n_group, w.topk_group, w.norm_topk_prob,
+                              w.routed_scaling_factor)
+        ties = near_tie_rows(lg, bias, w.top_k, w.n_group, w.topk_group)
+        check_route(inds.cpu().numpy(), scores.cpu().numpy(), ri, rs, ties)
+        rows = rows[~ties]
+    ref = oracle.moe_layer(xb, ri, rs, oracle_experts(data["experts"]),
+                           oracle_shared(data["shared"]), rows=rows,
+                           shared_gate=None if wsg is None else bits(wsg))
+    check_layer(y.float().cpu().numpy()[rows], ref)
+
+
+@pytest.mark.parametrize("T", [7, 64, 300, 520])
+@pytest.mark.parametrize("route_kind,gated", [(binding.MOE_ROUTE_SOFTMAX, False),
+                                              (binding.MOE_ROUTE_SOFTMAX, True),
+                                              (binding.MOE_ROUTE_DEEPSEEK, True)],
+                         ids=["softmax", "softmax_gated", "deepseek_gated"])
+def test_forward_ex_softmax_and_gated_shared(T, route_kind, gated):
+    w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=T)
+    data = inputs.gen_layer(w, DEV, seed=T + 3 * int(gated) + route_kind)
+    wsg = None
+    if gated:
+        g = torch.Generator(device=DEV).manual_seed(T)
+        wsg = (torch.randn(w.d, generator=g, device=DEV) / w.d ** 0.5).to(torch.bfloat16)
+    _check_forward_ex(w, data, route_kind, wsg)
+
+
+def test_shared_gate_and_combine_gated_parts():
+    w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=45)
+    data = inputs.gen_layer(w, DEV, seed=21)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    wsg = (torch.randn(w.d, generator=g, device=DEV) * 0.05).to(torch.bfloat16)
+    x = data["x"]
+    gate = binding.shared_gate(x, wsg)
+    torch.cuda.synchronize()
+    z = bits(x).astype(np.uint32) << 16
+    xf = z.view(np.float32).astype(np.float64)
+    wf = (bits(wsg).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref_gate = 1.0 / (1.0 + np.exp(-(xf @ wf)))
+    np.testing.assert_allclose(gate.cpu().numpy(), ref_gate, rtol=1e-5, atol=0)
+    lg = binding.router_logits(x, data["w_router"])
+    inds, scores = binding.route_softmax(lg, w.top_k)
+    counts, offsets, perm, inv = binding.permute(inds, w.E)
+    eo = binding.grouped_swiglu(x, offsets, perm, w.top_k, data["experts"], data["shared"])
+    P = w.T * w.top_k
+    y = binding.combine_gated(eo[:P], scores, inv, eo[P:], gate)
+    torch.cuda.synchronize()
+    ref = oracle.moe_layer(bits(x), inds.cpu().numpy(), scores.cpu().numpy(),
+                           oracle_experts(data["experts"]), oracle_shared(data["shared"]),
+                           shared_gate=bits(wsg))
+    check_layer(y.float().cpu().numpy(), ref)
+
+
+def test_forward_ex_rejects_bad_arguments():
+    w = inputs.WORKLOADS["tiny_T64_E16"]
+    data = inputs.gen_layer(w, DEV, seed=2)
+    wsg = torch.zeros(w.d, dtype=torch.bfloat16, device=DEV)
+    layer = binding.MoELayer(data["w_router"], None, data["experts"], None, w.top_k, 1, 1,
+                             True, 1.0, route_kind=binding.MOE_ROUTE_SOFTMAX, w_shared_gate=wsg)
+    with pytest.raises(binding.MoeError, match="without a shared expert"):
+        layer(data["x"])
+    layer = binding.MoELayer(data["w_router"], None, data["experts"], data["shared"], w.top_k,
+                             w.n_group, w.topk_group, True, 1.0,
+                             route_kind=binding.MOE_ROUTE_DEEPSEEK, w_shared_gate=wsg)
+    with pytest.raises(binding.MoeError, match="NULL"):
+        layer(data["x"])
+    torch.cuda.synchronize()
+
+
 def test_layer_empty_batch():
     w = inputs.WORKLOADS["tiny_T64_E16"]
     data = inputs.gen_layer(w, DEV, seed=0)

@@ -100,6 +100,49 @@ def test_route_rejection_leaves_outputs_untouched():
 
 
 # ------------------------------------------------------------------------------------
+# softmax route: top-K by logit, weights renormalised over the selection
+# ------------------------------------------------------------------------------------
+
+def _softmax_check(logits, K):
+    gi, gs = binding.route_softmax(logits, K)
+    torch.cuda.synchronize()
+    ri, rs = oracle.route_softmax(logits.float().cpu().numpy(), K)
+    assert np.array_equal(gi.cpu().numpy(), ri)
+    # both sides take exp in fp32; the library exponentials differ by a few ulp
+    np.testing.assert_allclose(gs.cpu().numpy(), rs, rtol=2e-6, atol=1e-12)
+    s = gs.cpu().numpy().sum(-1)
+    assert np.all(np.abs(s - 1) < 1e-5)
+    return gi, gs
+
+
+@pytest.mark.parametrize("E,K", [(8, 1), (16, 4), (60, 6), (64, 8), (128, 8), (256, 8),
+                                 (1024, 32), (5, 5)])
+def test_softmax_route_shapes(E, K):
+    g = torch.Generator(device=DEV).manual_seed(E * 17 + K)
+    _softmax_check(torch.randn(555, E, generator=g, device=DEV) * 3, K)
+
+
+def test_softmax_route_ties_and_bf16():
+    g = torch.Generator(device=DEV).manual_seed(9)
+    # integer logits: exact ties resolved to the lower expert index on both sides
+    gi, _ = _softmax_check(torch.randint(-2, 3, (300, 24), generator=g, device=DEV).float(), 5)
+    # all-equal logits: experts 0..K-1, each weight 1/K
+    gi, gs = _softmax_check(torch.zeros(4, 12, device=DEV), 3)
+    assert np.array_equal(gi.cpu().numpy(), np.tile(np.arange(3, dtype=np.int32), (4, 1)))
+    # bf16 logits with leading dimensions
+    _softmax_check((torch.randn(7, 9, 64, generator=g, device=DEV) * 2).to(torch.bfloat16), 4)
+
+
+def test_softmax_route_empty_and_rejection():
+    binding.route_softmax(torch.zeros(0, 16, device=DEV), 4)
+    inds = torch.full((5, 17), -7, dtype=torch.int32, device=DEV)
+    with pytest.raises(binding.MoeError):
+        binding.route_softmax(torch.zeros(5, 16, device=DEV), 17, inds=inds)
+    torch.cuda.synchronize()
+    assert torch.all(inds == -7)
+
+
+# ------------------------------------------------------------------------------------
 # dispatch
 # ------------------------------------------------------------------------------------
 
