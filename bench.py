@@ -42,10 +42,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # workload with the hash of the GEMM sources the capture ran; a stale hash reports null.
 # Captures: profiles/moe_gemm_gateup_dsv3_E32_T16.md, moe_gemm_gateup_dsv3_E32_T1024_zipf.md.
 NCU_TRAFFIC = {
-    "dsv3_T128": {"src": "c11937a8340574d2", "ratio": (1.705243e9 + 3.266304e6) / 1705541632},
-    "dsv3_T8192_zipf": {"src": "c11937a8340574d2",
-                        "ratio": (2.110998e9 + 27.3088e6) / (32 * 2 * 2048 * 7168 * 2
-                                                             + 9216 * (7168 + 2048) * 2)},
+    "dsv3_T128": {"src": "450af39e87434d9a", "ratio": (1.705382e9 + 4.040448e6) / 1705541632},
+    "dsv3_T8192_zipf": {"src": "450af39e87434d9a",
+                        "ratio": (2.067858e9 + 27.325696e6) / (32 * 2 * 2048 * 7168 * 2
+                                                               + 9216 * (7168 + 2048) * 2)},
 }
 
 
