@@ -25,7 +25,7 @@ EXPORTS = ("moe_last_error", "moe_version", "moe_device_status", "moe_route_deep
            "moe_grouped_swiglu_workspace_bytes", "moe_combine", "moe_forward",
            "moe_forward_workspace_bytes", "moe_set_phase_events", "moe_forward_noalloc",
            "moe_route_softmax", "moe_shared_gate", "moe_combine_gated", "moe_forward_ex",
-           "moe_forward_ex_workspace_bytes")
+           "moe_forward_ex_workspace_bytes", "moe_watchdog_selftest")
 MOE_ROUTE_DEEPSEEK, MOE_ROUTE_SOFTMAX = 0, 1
 
 
@@ -103,11 +103,12 @@ def lib(path: str | None = None):
             L.moe_forward_ex.argtypes = [ctypes.POINTER(LayerArgs), P, sz, P]
             L.moe_forward_ex_workspace_bytes.argtypes = [ctypes.POINTER(LayerArgs)]
             L.moe_forward_ex_workspace_bytes.restype = sz
+            L.moe_watchdog_selftest.argtypes = [i64, P]
             for name in ("moe_device_status", "moe_route_deepseek", "moe_permute",
                          "moe_router_logits", "moe_grouped_swiglu", "moe_combine",
                          "moe_forward", "moe_set_phase_events", "moe_forward_noalloc",
                          "moe_route_softmax", "moe_shared_gate", "moe_combine_gated",
-                         "moe_forward_ex"):
+                         "moe_forward_ex", "moe_watchdog_selftest"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -412,3 +413,9 @@ def set_phase_events(events):
 def device_status(clear=True, stream=None):
     """MOE_OK, or raises MoeError(MOE_ERR_TIMEOUT) if a kernel gave up a wait."""
     _check(lib().moe_device_status(int(bool(clear)), _stream(stream)))
+
+
+def watchdog_selftest(limit_ns=20_000_000, stream=None):
+    """Launches a wait that nothing completes, bounded by limit_ns; afterwards
+    device_status() raises MoeError(MOE_ERR_TIMEOUT)."""
+    _check(lib().moe_watchdog_selftest(int(limit_ns), _stream(stream)))

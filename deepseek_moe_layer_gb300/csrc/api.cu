@@ -415,6 +415,17 @@ int moe_device_status(int32_t clear, moe_stream_t stream) {
     return MOE_OK;
 }
 
+int moe_watchdog_selftest(int64_t limit_ns, moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(limit_ns >= 1000 && limit_ns <= 1000000000, "limit_ns = %lld outside [1e3, 1e9]",
+              (long long)limit_ns);
+    int rc = check_device();
+    if (rc) return rc;
+    MOE_CUDA(moe::launch_watchdog_selftest((unsigned long long)limit_ns, (cudaStream_t)stream),
+             "watchdog self-test kernel");
+    return MOE_OK;
+}
+
 int moe_route_deepseek(const void* logits, moe_dtype_t dtype, int64_t rows, int32_t E,
                        const float* bias, const moe_route_params_t* params, int32_t* inds,
                        float* scores, moe_stream_t stream) {

@@ -907,6 +907,29 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
 }
 
+namespace {
+// A single warp: lane 0 initialises an mbarrier expecting one arrival that never comes and
+// waits on it through mbar_wait with the given limit, exactly as a GEMM role waits on a
+// copy that never lands; when the wait gives up it records the timeout.
+__global__ void watchdog_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, &abort_flag, limit_ns))
+        record_timeout(&abort_flag);
+}
+}  // namespace
+
+cudaError_t launch_watchdog_selftest(unsigned long long limit_ns, cudaStream_t s) {
+    watchdog_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t read_device_status(unsigned int* out, int clear, cudaStream_t s) {
     cudaError_t err = cudaMemcpyFromSymbolAsync(out, g_status, sizeof(unsigned int), 0,
                                                 cudaMemcpyDeviceToHost, s);

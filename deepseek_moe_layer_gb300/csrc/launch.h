@@ -86,6 +86,8 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 
 // Per-device status word of the kernels with bounded waits.
 cudaError_t read_device_status(unsigned int* out, int clear, cudaStream_t s);
+// One CTA waits `limit_ns` on an mbarrier nothing completes and records the timeout.
+cudaError_t launch_watchdog_selftest(unsigned long long limit_ns, cudaStream_t s);
 
 int num_sms();
 

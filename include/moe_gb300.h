@@ -95,6 +95,13 @@ int32_t moe_version(void);
  * MOE_ERR_TIMEOUT.  Synchronises `stream` first. */
 int moe_device_status(int32_t clear, moe_stream_t stream);
 
+/* Exercises the device-side timeout path without a fault: one CTA waits on an mbarrier that
+ * nothing completes, through the same bounded wait the GEMM kernels use, gives up after
+ * limit_ns (1e3 <= limit_ns <= 1e9, else MOE_ERR_INVALID) and records MOE_ERR_TIMEOUT in the
+ * status word.  A following moe_device_status() must then report MOE_ERR_TIMEOUT, and the
+ * context stays usable.  Lets a deployment check the watchdog plumbing on its device. */
+int moe_watchdog_selftest(int64_t limit_ns, moe_stream_t stream);
+
 /*
  * moe_route_deepseek -- the DeepSeek gate ([gate] "API" and "Algorithm").
  *   logits [rows, E] (fp32 or bf16; any leading dims flattened to rows), bias [E] fp32

@@ -139,3 +139,59 @@ def test_binding_rejects_bad_bias_rank():
         binding.route_deepseek(lg, torch.zeros(1, 8), 2, 1, 1, True, 1.0)
     with pytest.raises(ValueError):
         binding.route_deepseek(lg, torch.zeros(7), 2, 1, 1, True, 1.0)
+
+
+def _forward_ex(route_kind=binding.MOE_ROUTE_SOFTMAX, bias=True, shared=True, gate=True,
+                top_k=4, E=16, ws_bytes=None):
+    L = binding.lib()
+    a = binding.LayerArgs()
+    a.route_kind, a.x, a.T, a.d, a.I, a.E = route_kind, 0x1000, 4, 256, 128, E
+    a.w_router = 0x1000
+    a.bias = 0x1000 if bias else None
+    a.params = binding.route_params(top_k, 4, 2, True, 2.5)
+    ew = binding.ExpertWeights(16, 0, 0x1000, 0x1000, 0x1000, None, None, None, None, None, None)
+    a.experts = ctypes.pointer(ew)
+    a.shared = ctypes.pointer(ew) if shared else None
+    a.w_shared_gate = 0x1000 if gate else None
+    a.y = 0x1000
+    need = L.moe_forward_ex_workspace_bytes(ctypes.byref(a))
+    rc = L.moe_forward_ex(ctypes.byref(a), ctypes.c_void_p(0x10000),
+                          need if ws_bytes is None else ws_bytes, None)
+    return rc, L.moe_last_error().decode(), need
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(route_kind=7), "route_kind 7"),
+    (dict(route_kind=binding.MOE_ROUTE_DEEPSEEK, bias=False), "NULL"),
+    (dict(top_k=17), "top_k = 17"),
+    (dict(E=2048, top_k=2), "E = 2048"),
+    (dict(shared=False), "without a shared expert"),
+    (dict(ws_bytes=4096), "ws_bytes"),
+])
+def test_forward_ex_validation_matrix(kw, msg):
+    rc, err, _ = _forward_ex(**kw)
+    assert rc == binding.MOE_ERR_INVALID
+    assert msg in err
+
+
+def test_forward_ex_workspace_counts_the_gate():
+    _, _, with_gate = _forward_ex(gate=True, ws_bytes=0)
+    _, _, without = _forward_ex(gate=False, ws_bytes=0)
+    assert with_gate == without + 256  # T = 4 fp32 gates, 256-byte aligned
+    assert without == binding.lib().moe_forward_workspace_bytes(4, 256, 128, 16, 4, 1)
+
+
+def test_softmax_gate_watchdog_validation():
+    L = binding.lib()
+    assert L.moe_route_softmax(FAKE, 0, 4, 16, 17, FAKE, FAKE, None) == binding.MOE_ERR_INVALID
+    assert "top_k = 17" in L.moe_last_error().decode()
+    assert L.moe_route_softmax(FAKE, 5, 4, 16, 2, FAKE, FAKE, None) == binding.MOE_ERR_INVALID
+    assert L.moe_route_softmax(None, 0, 4, 16, 2, FAKE, FAKE, None) == binding.MOE_ERR_INVALID
+    assert L.moe_route_softmax(None, 0, 0, 16, 2, None, None, None) == binding.MOE_OK
+    assert L.moe_shared_gate(FAKE, 4, 100, FAKE, FAKE, None) == binding.MOE_ERR_INVALID
+    assert L.moe_shared_gate(FAKE, 4, 256, None, FAKE, None) == binding.MOE_ERR_INVALID
+    assert L.moe_combine_gated(FAKE, FAKE, FAKE, FAKE, None, 4, 2, 256, FAKE,
+                               None) == binding.MOE_ERR_INVALID
+    for bad in (0, 999, 2_000_000_000):
+        assert L.moe_watchdog_selftest(bad, None) == binding.MOE_ERR_INVALID
+        assert "limit_ns" in L.moe_last_error().decode()
