@@ -70,6 +70,8 @@ def _load():
             lib.oracle_bf16_to_f32.restype = f32
             lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
             lib.oracle_f16_to_f32.restype = f32
+            lib.oracle_indexer_topk.argtypes = [P, i64, i32, i64, P, i32, P, P, i64]
+            lib.oracle_indexer_topk.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -157,6 +159,24 @@ def route_softmax(logits, top_k):
     if lib.oracle_route_softmax(_ptr(lg), rows, E, top_k, _ptr(inds), _ptr(scores)) != 0:
         raise ValueError("oracle_route_softmax rejected its arguments")
     return inds, scores
+
+
+def indexer_topk(scores, k, lengths=None, want_mask=False):
+    """DSA indexer selection on fp32 scores [rows, n]: int32 [rows, k] positions of the
+    min(k, n_r) largest valid scores (positions j < n_r, n_r = lengths[r] or n), ascending,
+    padded with -1; with want_mask also the uint8 [rows, n] mask of the selection."""
+    lib = _load()
+    sc = _c(scores, np.float32)
+    if sc.ndim != 2:
+        raise ValueError("scores must be [rows, n]")
+    rows, n = sc.shape
+    ln = None if lengths is None else _c(lengths, np.int32)
+    inds = np.zeros((rows, k), np.int32)
+    mask = np.zeros((rows, n), np.uint8) if want_mask else None
+    if lib.oracle_indexer_topk(_ptr(sc), rows, n, n, _ptr(ln), k, _ptr(inds), _ptr(mask),
+                               n) != 0:
+        raise ValueError("oracle_indexer_topk rejected its arguments")
+    return (inds, mask) if want_mask else inds
 
 
 def moe_layer(x_bits, inds, scores, experts, shared=None, rows=None, group=64,
