@@ -25,7 +25,7 @@ EXPORTS = ("moe_last_error", "moe_version", "moe_device_status", "moe_route_deep
            "moe_grouped_swiglu_workspace_bytes", "moe_combine", "moe_forward",
            "moe_forward_workspace_bytes", "moe_set_phase_events", "moe_forward_noalloc",
            "moe_route_softmax", "moe_shared_gate", "moe_combine_gated", "moe_forward_ex",
-           "moe_forward_ex_workspace_bytes", "moe_watchdog_selftest")
+           "moe_forward_ex_workspace_bytes", "moe_watchdog_selftest", "moe_indexer_topk")
 MOE_ROUTE_DEEPSEEK, MOE_ROUTE_SOFTMAX = 0, 1
 
 
@@ -104,11 +104,12 @@ def lib(path: str | None = None):
             L.moe_forward_ex_workspace_bytes.argtypes = [ctypes.POINTER(LayerArgs)]
             L.moe_forward_ex_workspace_bytes.restype = sz
             L.moe_watchdog_selftest.argtypes = [i64, P]
+            L.moe_indexer_topk.argtypes = [P, ctypes.c_int, i64, i32, i64, P, i32, P, P, i64, P]
             for name in ("moe_device_status", "moe_route_deepseek", "moe_permute",
                          "moe_router_logits", "moe_grouped_swiglu", "moe_combine",
                          "moe_forward", "moe_set_phase_events", "moe_forward_noalloc",
                          "moe_route_softmax", "moe_shared_gate", "moe_combine_gated",
-                         "moe_forward_ex", "moe_watchdog_selftest"):
+                         "moe_forward_ex", "moe_watchdog_selftest", "moe_indexer_topk"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -237,6 +238,32 @@ def combine_gated(expert_out, scores, inv_perm, shared_out, gate, stream=None):
                                    _ptr(shared_out), _ptr(gate), T, K, d, _ptr(y),
                                    _stream(stream)))
     return y
+
+
+def indexer_topk(scores, k, lengths=None, want_mask=False, inds=None, mask=None,
+                 stream=None):
+    """DSA indexer selection: scores [rows, n] fp32/bf16 (rows may be strided: the row
+    stride is taken from the tensor) -> int32 [rows, k] ascending positions padded with -1,
+    and with want_mask also the uint8 [rows, n] selection mask."""
+    if scores.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("scores must be fp32 or bf16")
+    if scores.dim() != 2 or (scores.shape[1] > 1 and scores.stride(1) != 1):
+        raise ValueError("scores must be [rows, n] with unit stride along n")
+    rows, n = scores.shape
+    ld = scores.stride(0) if rows > 1 else n
+    if lengths is not None:
+        _need(lengths, torch.int32, "lengths", scores.device)
+        if lengths.shape != (rows,):
+            raise ValueError("lengths must be [rows]")
+    if inds is None:
+        inds = torch.empty(rows, int(k), dtype=torch.int32, device=scores.device)
+    if want_mask and mask is None:
+        mask = torch.empty(rows, n, dtype=torch.uint8, device=scores.device)
+    dt = MOE_DTYPE_F32 if scores.dtype == torch.float32 else MOE_DTYPE_BF16
+    _check(lib().moe_indexer_topk(_ptr(scores), dt, rows, n, ld, _ptr(lengths), int(k),
+                                  _ptr(inds), _ptr(mask), n if mask is not None else 0,
+                                  _stream(stream)))
+    return (inds, mask) if want_mask else inds
 
 
 def permute(inds, E, stream=None):

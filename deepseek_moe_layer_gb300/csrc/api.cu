@@ -415,6 +415,36 @@ int moe_device_status(int32_t clear, moe_stream_t stream) {
     return MOE_OK;
 }
 
+int moe_indexer_topk(const void* scores, moe_dtype_t dtype, int64_t rows, int32_t n,
+                     int64_t ld, const int32_t* lengths, int32_t k, int32_t* inds,
+                     uint8_t* mask, int64_t mask_ld, moe_stream_t stream) {
+    g_err.clear();
+    MOE_CHECK(dtype == MOE_DTYPE_F32 || dtype == MOE_DTYPE_BF16, "dtype %d unknown", (int)dtype);
+    MOE_CHECK(rows >= 0, "rows = %lld < 0", (long long)rows);
+    MOE_CHECK(n >= 0, "n = %d < 0", n);
+    MOE_CHECK(ld >= n, "ld = %lld < n = %d", (long long)ld, n);
+    MOE_CHECK(k >= 1 && k <= (1 << 20), "k = %d outside [1, 2^20]", k);
+    MOE_CHECK(!mask || mask_ld >= n, "mask_ld = %lld < n = %d", (long long)mask_ld, n);
+    MOE_CHECK(rows == 0 || (inds && (n == 0 || scores)), "NULL pointer argument");
+    if (rows == 0) return MOE_OK;
+    int rc = check_device();
+    if (rc) return rc;
+    moe::TopkArgs a = {};
+    a.scores = scores;
+    a.bf16 = dtype == MOE_DTYPE_BF16;
+    a.rows = rows;
+    a.n = n;
+    a.ld = ld;
+    a.lengths = lengths;
+    a.k = k;
+    a.inds = inds;
+    a.mask = mask;
+    a.mask_ld = mask_ld;
+    moe::indexer_topk_plan(a);
+    MOE_CUDA(moe::launch_indexer_topk(a, (cudaStream_t)stream), "indexer top-k kernel");
+    return MOE_OK;
+}
+
 int moe_watchdog_selftest(int64_t limit_ns, moe_stream_t stream) {
     g_err.clear();
     MOE_CHECK(limit_ns >= 1000 && limit_ns <= 1000000000, "limit_ns = %lld outside [1e3, 1e9]",

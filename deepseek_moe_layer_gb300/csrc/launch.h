@@ -46,6 +46,28 @@ cudaError_t launch_combine(const void* expert_out, const float* scores, const in
 cudaError_t launch_shared_gate(const void* x, long long T, int d, const void* w, float* gate,
                                cudaStream_t s);
 
+// ---- DSA indexer top-k selection -----------------------------------------------------
+struct TopkArgs {
+    const void* scores;          // [rows, ld] fp32, or bf16 when bf16 != 0
+    int bf16;
+    long long rows;
+    int n;                       // positions per row
+    long long ld;                // elements between rows (>= n)
+    const int32_t* lengths;      // [rows] valid positions per row, or nullptr (all n)
+    int k;                       // index_topk
+    int32_t* inds;               // [rows, k] selected positions, ascending, -1 padded
+    uint8_t* mask;               // [rows, mask_ld] 1 at the selected positions, or nullptr
+    long long mask_ld;
+    int nclusters;               // CTAs per row (thread-block cluster size, 1..8)
+    int seg;                     // positions per CTA (multiple of 8)
+    int cached;                  // keys of a segment held in shared memory
+};
+// Fills nclusters / seg / cached from n.
+void indexer_topk_plan(TopkArgs& a);
+// Per-CTA dynamic shared memory of the selection kernel.
+size_t indexer_topk_smem(int seg, int cached);
+cudaError_t launch_indexer_topk(const TopkArgs& a, cudaStream_t s);
+
 // ---- expert GEMMs (tcgen05) ---------------------------------------------------------
 enum GemmMode { kGateUp = 0, kDown = 1, kRouter = 2 };
 

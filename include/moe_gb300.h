@@ -95,6 +95,26 @@ int32_t moe_version(void);
  * MOE_ERR_TIMEOUT.  Synchronises `stream` first. */
 int moe_device_status(int32_t clear, moe_stream_t stream);
 
+/*
+ * moe_indexer_topk -- the DSA indexer's selection (SwiftLM issue #139, "What needs
+ * building" items 1 and 3: argPartition(scores, kth: -index_topk); decode gathers the
+ * selected positions, prefill ANDs them into the causal mask).
+ *   scores [rows, ld] fp32 or bf16, n positions per row (ld >= n, in elements).
+ *   lengths [rows] int32 or NULL: row r considers positions j < lengths[r] only (clamped to
+ *     [0, n]; the causal length of a prefill query); NULL means n for every row.
+ *   k = index_topk (1 <= k <= 2^20).
+ *   Out: inds [rows, k] int32: the positions of the min(k, n_r) largest scores of the row,
+ *     larger score first and equal scores by lower position (NaN lowest, -0 == +0),
+ *     written in ASCENDING position order and padded with -1.  A row with n_r <= k selects
+ *     all its positions (the inert regime: identical to dense attention).
+ *   mask [rows, mask_ld] uint8 or NULL (mask_ld >= n): 1 at the selected positions, 0 at
+ *     every other position j < n (the selection already excludes j >= n_r).
+ *   Exact: positions are chosen by comparisons only, no arithmetic on the scores.
+ */
+int moe_indexer_topk(const void* scores, moe_dtype_t dtype, int64_t rows, int32_t n,
+                     int64_t ld, const int32_t* lengths, int32_t k, int32_t* inds,
+                     uint8_t* mask, int64_t mask_ld, moe_stream_t stream);
+
 /* Exercises the device-side timeout path without a fault: one CTA waits on an mbarrier that
  * nothing completes, through the same bounded wait the GEMM kernels use, gives up after
  * limit_ns (1e3 <= limit_ns <= 1e9, else MOE_ERR_INVALID) and records MOE_ERR_TIMEOUT in the
