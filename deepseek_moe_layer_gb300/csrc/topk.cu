@@ -11,12 +11,13 @@
 //
 // Design: one thread-block cluster per row (1..8 CTAs, each a contiguous segment of the
 // row).  Scores become order-preserving 32-bit keys, cached in shared memory.  A radix
-// select over three digits (11, 11, 10 bits) finds the key of the k-th largest element: each
-// pass builds a per-CTA histogram of the digit over the keys that still match the chosen
-// prefix (warp-aggregated shared-memory atomics), the cluster's histograms are summed over
-// distributed shared memory, and every CTA picks the same digit.  The final pass compacts the
-// selected positions in position order with block scans; elements equal to the threshold key
-// are taken lowest position first, across the cluster's segments in order.
+// select finds the key of the k-th largest element digit by digit (11-bit digits for long
+// rows, 8-bit for short ones): each pass builds a per-CTA histogram of the digit over the keys
+// that still match the chosen prefix (shared-memory atomics; warp pre-aggregation with
+// match.any measured slower), the cluster's histograms are summed over distributed shared
+// memory, and every CTA picks the same digit.  The last pass compacts the selected positions
+// in position order (each warp a contiguous range, ballot-free lane scans); elements equal to
+// the threshold key are taken lowest position first, across the cluster's segments in order.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -27,9 +28,6 @@ namespace {
 
 namespace cg = cooperative_groups;
 
-constexpr int kTkThreads = 512;
-constexpr int kTkWarps = kTkThreads / 32;
-constexpr int kBins = 2048;  // histogram size of the 11-bit digits
 constexpr unsigned kAll = 0xFFFFFFFFu;
 
 // Order-preserving key of an fp32 score: NaN -> 0 (lowest), -0 -> +0.
@@ -49,8 +47,10 @@ MOE_DEV uint32_t load_key(const void* base, long long j) {
     return score_key(static_cast<const float*>(base)[j]);
 }
 
-// Exclusive block-wide prefix sum of v (all kTkThreads threads call it); *total gets the sum.
+// Exclusive block-wide prefix sum of v over THREADS threads (all call it); *total = sum.
+template <int THREADS>
 MOE_DEV uint32_t block_excl_scan(uint32_t v, uint32_t* s_warp, uint32_t* total) {
+    constexpr int W = THREADS / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t x = v;
 #pragma unroll
@@ -61,36 +61,53 @@ MOE_DEV uint32_t block_excl_scan(uint32_t v, uint32_t* s_warp, uint32_t* total) 
     if (lane == 31) s_warp[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        uint32_t w = lane < kTkWarps ? s_warp[lane] : 0u;
+        uint32_t w = lane < W ? s_warp[lane] : 0u;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(kAll, w, o);
             if (lane >= o) w += y;
         }
-        if (lane < kTkWarps) s_warp[lane] = w;  // inclusive warp totals
+        if (lane < W) s_warp[lane] = w;  // inclusive warp totals
     }
     __syncthreads();
     const uint32_t before = (warp ? s_warp[warp - 1] : 0u) + x - v;
-    *total = s_warp[kTkWarps - 1];
+    *total = s_warp[W - 1];
     __syncthreads();  // s_warp is reused by the next call
     return before;
 }
 
-template <bool BF16>
-__global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const TopkArgs a) {
+// Four consecutive keys from shared memory starting at i (a multiple of 4); keys at or past
+// `end` read as 0 and are flagged invalid by the caller.
+MOE_DEV uint4 keys4(const uint32_t* keys, int i, int end) {
+    if (i + 3 < end) return *reinterpret_cast<const uint4*>(keys + i);
+    uint4 q;
+    q.x = i < end ? keys[i] : 0u;
+    q.y = i + 1 < end ? keys[i + 1] : 0u;
+    q.z = i + 2 < end ? keys[i + 2] : 0u;
+    q.w = 0u;
+    return q;
+}
+
+// THREADS threads per CTA; digits of DBITS bits (the last pass takes the remaining bits).
+template <bool BF16, int THREADS, int DBITS>
+__global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a) {
+    constexpr int W = THREADS / 32;
+    constexpr int NB = 1 << DBITS;
+    constexpr int NPASS = (32 + DBITS - 1) / DBITS;
     cg::cluster_group cl = cg::this_cluster();
     const unsigned nc = cl.num_blocks();
     const unsigned rank = cl.block_rank();
     const long long row = (long long)(blockIdx.x / nc);
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     extern __shared__ __align__(16) uint8_t tk_smem[];
-    int* hist = reinterpret_cast<int*>(tk_smem);            // [kBins] this CTA's histogram
-    int* merged = hist + kBins;                              // [kBins] the cluster's sum
-    uint32_t* keys = reinterpret_cast<uint32_t*>(merged + kBins);  // [seg] when cached
-    __shared__ uint32_t s_warp[kTkWarps];
-    __shared__ int s_pick[2];       // chosen digit, remaining count
-    __shared__ int s_counts[2];     // this CTA's (greater, equal) counts, read by the cluster
+    int* hist = reinterpret_cast<int*>(tk_smem);                  // [NB] this CTA's histogram
+    int* merged = hist + NB;                                       // [NB] the cluster's sum
+    uint32_t* keys = reinterpret_cast<uint32_t*>(merged + NB);     // [seg] when cached
+    __shared__ uint32_t s_warp[W];
+    __shared__ uint32_t s_wg[W], s_wq[W];  // per-warp greater / equal counts, then prefixes
+    __shared__ int s_pick[2];               // chosen digit, remaining count
+    __shared__ int s_counts[2];             // this CTA's (greater, equal) counts
 
     const int n = a.n, k = a.k;
     int nr = a.lengths ? a.lengths[row] : n;
@@ -101,15 +118,27 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const TopkArgs
     const int cnt = v1 > j0 ? v1 - j0 : 0;  // valid positions of this CTA's segment
     int32_t* out = a.inds + row * (long long)k;
     uint8_t* mrow = a.mask ? a.mask + row * a.mask_ld : nullptr;
+    const bool mvec = mrow && ((reinterpret_cast<uintptr_t>(mrow + j0) & 3u) == 0);
 
     if (nr <= k) {
         // every valid position is selected: position j goes to slot j, the rest are -1
-        for (int j = j0 + tid; j < j1; j += kTkThreads) {
-            if (j < nr) out[j] = j;
-            if (mrow) mrow[j] = j < nr ? 1 : 0;
-        }
+        for (int j = j0 + tid; j < v1; j += THREADS) out[j] = j;
         if (rank == 0)
-            for (int p = nr + tid; p < k; p += kTkThreads) out[p] = -1;
+            for (int p = nr + tid; p < k; p += THREADS) out[p] = -1;
+        if (mrow) {
+            if (mvec) {
+                for (int j = j0 + 4 * tid; j < j1; j += 4 * THREADS) {
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) m |= (uint32_t)(j + e < nr) << (8 * e);
+                    if (j + 3 < j1) *reinterpret_cast<uint32_t*>(mrow + j) = m;
+                    else
+                        for (int e = 0; j + e < j1; ++e) mrow[j + e] = j + e < nr ? 1 : 0;
+                }
+            } else {
+                for (int j = j0 + tid; j < j1; j += THREADS) mrow[j] = j < nr ? 1 : 0;
+            }
+        }
         return;  // no distributed shared memory was touched: CTAs may leave independently
     }
 
@@ -123,60 +152,105 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const TopkArgs
                                (uintptr_t)j0 * (BF16 ? 2u : 4u);
         const bool vec = (addr & 15u) == 0;
         const int nv = vec ? cnt / per : 0;
-        for (int v = tid; v < nv; v += kTkThreads) {
+        for (int v = tid; v < nv; v += THREADS) {
             const uint4 q = reinterpret_cast<const uint4*>(addr)[v];
             const uint32_t w[4] = {q.x, q.y, q.z, q.w};
             if (BF16) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    keys[v * 8 + 2 * e] = score_key(__uint_as_float(w[e] << 16));
-                    keys[v * 8 + 2 * e + 1] = score_key(__uint_as_float(w[e] & 0xFFFF0000u));
-                }
+                uint4 lo, hi;
+                lo.x = score_key(__uint_as_float(w[0] << 16));
+                lo.y = score_key(__uint_as_float(w[0] & 0xFFFF0000u));
+                lo.z = score_key(__uint_as_float(w[1] << 16));
+                lo.w = score_key(__uint_as_float(w[1] & 0xFFFF0000u));
+                hi.x = score_key(__uint_as_float(w[2] << 16));
+                hi.y = score_key(__uint_as_float(w[2] & 0xFFFF0000u));
+                hi.z = score_key(__uint_as_float(w[3] << 16));
+                hi.w = score_key(__uint_as_float(w[3] & 0xFFFF0000u));
+                reinterpret_cast<uint4*>(keys)[2 * v] = lo;
+                reinterpret_cast<uint4*>(keys)[2 * v + 1] = hi;
             } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) keys[v * 4 + e] = score_key(__uint_as_float(w[e]));
+                uint4 kq;
+                kq.x = score_key(__uint_as_float(w[0]));
+                kq.y = score_key(__uint_as_float(w[1]));
+                kq.z = score_key(__uint_as_float(w[2]));
+                kq.w = score_key(__uint_as_float(w[3]));
+                reinterpret_cast<uint4*>(keys)[v] = kq;
             }
         }
-        for (int i = nv * per + tid; i < cnt; i += kTkThreads)
-            keys[i] = load_key<BF16>(srow, j0 + i);
+        for (int i = nv * per + tid; i < cnt; i += THREADS) keys[i] = load_key<BF16>(srow, j0 + i);
     }
     __syncthreads();
 
+    // four keys of this CTA's segment starting at i (a multiple of 4)
+    auto get4 = [&](int i) -> uint4 {
+        if (cached) return keys4(keys, i, cnt);
+        uint4 q;
+        q.x = i < cnt ? load_key<BF16>(srow, j0 + i) : 0u;
+        q.y = i + 1 < cnt ? load_key<BF16>(srow, j0 + i + 1) : 0u;
+        q.z = i + 2 < cnt ? load_key<BF16>(srow, j0 + i + 2) : 0u;
+        q.w = i + 3 < cnt ? load_key<BF16>(srow, j0 + i + 3) : 0u;
+        return q;
+    };
+    auto csync = [&]() {
+        if (nc > 1) cl.sync();
+        else __syncthreads();
+    };
+
     // ---- radix select of the k-th largest key over the cluster ----
     uint32_t prefix = 0, pmask = 0;
-    int kk = k;  // elements still to take among those matching the prefix
+    int kk = k;           // elements still to take among those matching the prefix
+    uint32_t my_gt = 0;   // this thread's share of the CTA's count of keys above the result
+    int last_digit = 0;
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const int nb = pass == 2 ? 1024 : 2048;
-        for (int b = tid; b < kBins; b += kTkThreads) hist[b] = 0;
+    for (int pass = 0; pass < NPASS; ++pass) {
+        const int top = 32 - DBITS * pass;
+        const int shift = top > DBITS ? top - DBITS : 0;
+        const int nb = 1 << (top - shift);
+        for (int b = tid; b < nb; b += THREADS) hist[b] = 0;
         __syncthreads();
-        for (int base = 0; base < cnt; base += kTkThreads) {
-            const int i = base + tid;
-            uint32_t key = 0;
-            if (i < cnt) key = cached ? keys[i] : load_key<BF16>(srow, j0 + i);
-            const bool want = i < cnt && (key & pmask) == prefix;
-            const uint32_t bin = (key >> shift) & (uint32_t)(nb - 1);
-            const unsigned grp = __match_any_sync(kAll, want ? bin : 0xFFFFFFFFu);
-            if (want && lane == __ffs(grp) - 1) atomicAdd(&hist[bin], __popc(grp));
+        for (int base = 0; base < cnt; base += 4 * THREADS) {
+            const int i = base + 4 * tid;
+            const uint4 q = get4(i);
+            const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+            bool want[4];
+            bool any = false;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                want[e] = i + e < cnt && (kq[e] & pmask) == prefix;
+                any |= want[e];
+            }
+            if (pass == 0 || __any_sync(kAll, any)) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t bin = (kq[e] >> shift) & (uint32_t)(nb - 1);
+                    if (want[e]) atomicAdd(&hist[bin], 1);
+                }
+            }
         }
-        cl.sync();  // every CTA's histogram is complete
-        for (int b = tid; b < nb; b += kTkThreads) {
-            int s = 0;
-            for (unsigned c = 0; c < nc; ++c) s += c == rank ? hist[b] : cl.map_shared_rank(hist, c)[b];
-            merged[b] = s;
+        const int* tot = hist;
+        if (nc > 1) {
+            cl.sync();  // every CTA's histogram is complete
+            for (int b = tid; b < nb; b += THREADS) {
+                int sum = 0;
+                for (unsigned c = 0; c < nc; ++c)
+                    sum += c == rank ? hist[b] : cl.map_shared_rank(hist, c)[b];
+                merged[b] = sum;
+            }
+            cl.sync();  // no CTA reads another's histogram any more
+            tot = merged;
+        } else {
+            __syncthreads();
         }
-        cl.sync();  // no CTA reads another's histogram any more
-        // digit: the bin where the count of larger digits < kk <= that count plus the bin
-        const int per = nb / kTkThreads;  // 4 or 2 bins per thread, thread t owns the top-down
-        const int hi = nb - 1 - tid * per;  // chunk [hi - per + 1, hi]
+        // digit: the bin where the count of larger digits < kk <= that count plus the bin;
+        // thread t owns bins hi, hi-1, .., hi-per+1 (top-down), hi = nb - 1 - t*per
+        const int per = nb >= THREADS ? nb / THREADS : 1;
+        const int hi = nb - 1 - tid * per;
         uint32_t mine = 0;
-        for (int q = 0; q < per; ++q) mine += (uint32_t)merged[hi - q];
+        for (int q = 0; q < per && hi - q >= 0; ++q) mine += (uint32_t)tot[hi - q];
         uint32_t total;
-        const uint32_t above = block_excl_scan(mine, s_warp, &total);
+        const uint32_t above = block_excl_scan<THREADS>(mine, s_warp, &total);
         uint32_t acc = above;
-        for (int q = 0; q < per; ++q) {
-            const uint32_t c = (uint32_t)merged[hi - q];
+        for (int q = 0; q < per && hi - q >= 0; ++q) {
+            const uint32_t c = (uint32_t)tot[hi - q];
             if (acc < (uint32_t)kk && acc + c >= (uint32_t)kk) {
                 s_pick[0] = hi - q;
                 s_pick[1] = kk - (int)acc;
@@ -184,64 +258,124 @@ __global__ void __launch_bounds__(kTkThreads) indexer_topk_kernel(const TopkArgs
             acc += c;
         }
         __syncthreads();
-        prefix |= (uint32_t)s_pick[0] << shift;
+        const int d = s_pick[0];
+        // this CTA's keys in the bins above the digit are above the final threshold
+        for (int q = 0; q < per && hi - q > d; ++q) my_gt += (uint32_t)hist[hi - q];
+        prefix |= (uint32_t)d << shift;
         pmask |= (uint32_t)(nb - 1) << shift;
         kk = s_pick[1];
+        last_digit = d;
         __syncthreads();
     }
     const uint32_t tau = prefix;  // key of the k-th largest; kk of the keys equal to it are taken
 
-    // ---- counts per CTA, then each CTA's share of the threshold ties and its output base ----
-    uint32_t gt = 0, eq = 0;
-    for (int i = tid; i < cnt; i += kTkThreads) {
-        const uint32_t key = cached ? keys[i] : load_key<BF16>(srow, j0 + i);
-        gt += key > tau;
-        eq += key == tau;
-    }
-    uint32_t tot_gt, tot_eq;
-    block_excl_scan(gt, s_warp, &tot_gt);
-    block_excl_scan(eq, s_warp, &tot_eq);
+    // ---- this CTA's counts, its share of the threshold ties and its output base ----
+    uint32_t cta_gt;
+    block_excl_scan<THREADS>(my_gt, s_warp, &cta_gt);
     if (tid == 0) {
-        s_counts[0] = (int)tot_gt;
-        s_counts[1] = (int)tot_eq;
+        s_counts[0] = (int)cta_gt;
+        s_counts[1] = hist[last_digit];  // keys equal to tau in this CTA
     }
-    cl.sync();
     int rem = kk, out_base = 0, take = 0;
-    for (unsigned c = 0; c < nc; ++c) {
-        const int* rc = c == rank ? s_counts : cl.map_shared_rank(s_counts, c);
-        const int g = rc[0], e = rc[1];
-        const int t = e < rem ? e : rem;
-        if (c < rank) out_base += g + t;
-        if (c == rank) take = t;
-        rem -= t;
+    if (nc > 1) {
+        cl.sync();
+        for (unsigned c = 0; c < nc; ++c) {
+            const int* rc = c == rank ? s_counts : cl.map_shared_rank(s_counts, c);
+            const int g = rc[0], e = rc[1];
+            const int t = e < rem ? e : rem;
+            if (c < rank) out_base += g + t;
+            if (c == rank) take = t;
+            rem -= t;
+        }
+        cl.sync();  // remote counts read: no CTA touches another's shared memory from here on
+    } else {
+        __syncthreads();
+        take = s_counts[1] < rem ? s_counts[1] : rem;
     }
-    cl.sync();  // remote counts read: from here on no CTA touches another's shared memory
 
-    // ---- compaction in position order ----
-    uint32_t gt_run = 0, eq_run = 0;
-    for (int base = 0; base < cnt; base += kTkThreads) {
-        const int i = base + tid;
-        uint32_t key = 0;
-        if (i < cnt) key = cached ? keys[i] : load_key<BF16>(srow, j0 + i);
-        const uint32_t g = (i < cnt) && key > tau;
-        const uint32_t e = (i < cnt) && key == tau;
-        uint32_t chunk;
-        // per-chunk counts are at most kTkThreads: both fit one word
-        const uint32_t before = block_excl_scan(g | (e << 16), s_warp, &chunk);
-        const uint32_t gb = gt_run + (before & 0xFFFFu);
-        const uint32_t eb = eq_run + (before >> 16);  // equal keys before this position
-        const bool sel = g || (e && eb < (uint32_t)take);
-        const uint32_t pos = (uint32_t)out_base + gb + min(eb, (uint32_t)take);
-        if (sel && pos < (uint32_t)k) out[pos] = j0 + i;  // exactly k are selected
-        if (mrow && i < cnt) mrow[j0 + i] = sel ? 1 : 0;
-        gt_run += chunk & 0xFFFFu;
-        eq_run += chunk >> 16;
+    // ---- compaction in position order: each warp a contiguous range, 4 keys per lane ----
+    const int wlen = ((cnt + W - 1) / W + 127) / 128 * 128;
+    const int w_lo = min(cnt, warp * wlen), w_hi = min(cnt, w_lo + wlen);
+    uint32_t wg = 0, wq = 0;
+    for (int b = w_lo; b < w_hi; b += 128) {
+        const int i = b + 4 * lane;
+        const uint4 q = i < w_hi ? get4(i) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const bool v = i + e < w_hi;
+            wg += v && kq[e] > tau;
+            wq += v && kq[e] == tau;
+        }
     }
-    if (mrow)  // positions of this segment past the row's valid length
-        for (int j = (v1 > j0 ? v1 : j0) + tid; j < j1; j += kTkThreads) mrow[j] = 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        wg += __shfl_xor_sync(kAll, wg, o);
+        wq += __shfl_xor_sync(kAll, wq, o);
+    }
+    if (lane == 0) { s_wg[warp] = wg; s_wq[warp] = wq; }
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t g = 0, e = 0;
+        for (int w = 0; w < W; ++w) {
+            const uint32_t tg = s_wg[w], te = s_wq[w];
+            s_wg[w] = g; s_wq[w] = e;
+            g += tg; e += te;
+        }
+    }
+    __syncthreads();
+    uint32_t g_run = s_wg[warp], q_run = s_wq[warp];
+    for (int b = w_lo; b < w_hi; b += 128) {
+        const int i = b + 4 * lane;
+        const uint4 q = i < w_hi ? get4(i) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+        uint32_t fg = 0, fq = 0;  // bit e: key e is above / equal to the threshold
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const bool v = i + e < w_hi;
+            fg |= (uint32_t)(v && kq[e] > tau) << e;
+            fq |= (uint32_t)(v && kq[e] == tau) << e;
+        }
+        // lanes' exclusive prefix of (equal, greater) counts within this 128-key step
+        const uint32_t packed = (uint32_t)__popc(fg) | ((uint32_t)__popc(fq) << 16);
+        uint32_t x = packed;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kAll, x, o);
+            if (lane >= o) x += y;
+        }
+        const uint32_t step_tot = __shfl_sync(kAll, x, 31);
+        const uint32_t before = x - packed;
+        uint32_t gb = g_run + (before & 0xFFFFu), qb = q_run + (before >> 16);
+        uint32_t mbits = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const bool isg = (fg >> e) & 1u, isq = (fq >> e) & 1u;
+            const bool sel = isg || (isq && qb < (uint32_t)take);
+            const uint32_t pos = (uint32_t)out_base + gb + min(qb, (uint32_t)take);
+            if (sel && pos < (uint32_t)k) out[pos] = j0 + i + e;  // exactly k are selected
+            mbits |= (uint32_t)sel << (8 * e);
+            gb += isg;
+            qb += isq;
+        }
+        if (mrow && i < w_hi) {
+            if (mvec && i + 3 < w_hi) *reinterpret_cast<uint32_t*>(mrow + j0 + i) = mbits;
+            else
+                for (int e = 0; e < 4 && i + e < w_hi; ++e)
+                    mrow[j0 + i + e] = (uint8_t)((mbits >> (8 * e)) & 1u);
+        }
+        g_run += step_tot & 0xFFFFu;
+        q_run += step_tot >> 16;
+    }
+    if (mrow) {  // positions of this segment past the row's valid length
+        const int z0 = v1 > j0 ? v1 : j0;
+        for (int j = z0 + tid; j < j1; j += THREADS) mrow[j] = 0;
+    }
 }
 
 }  // namespace
+
+constexpr int kShortRow = 8192;  // segments up to this many keys take the short-row kernel
 
 void indexer_topk_plan(TopkArgs& a) {
     // segments of at most kSegMax keys (64 KB of shared memory) per CTA, up to 8 CTAs per
@@ -257,15 +391,17 @@ void indexer_topk_plan(TopkArgs& a) {
 }
 
 size_t indexer_topk_smem(int seg, int cached) {
-    return (size_t)2 * kBins * sizeof(int) + (cached ? (size_t)seg * sizeof(uint32_t) : 0);
+    const int nb = seg <= kShortRow ? 256 : 2048;
+    return (size_t)2 * nb * sizeof(int) + (cached ? (size_t)seg * sizeof(uint32_t) : 0);
 }
 
-cudaError_t launch_indexer_topk(const TopkArgs& a, cudaStream_t s) {
-    if (a.rows == 0) return cudaSuccess;
+namespace {
+template <bool BF16, int THREADS, int DBITS>
+cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
     const size_t smem = indexer_topk_smem(a.seg, a.cached);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.rows * a.nclusters), 1, 1);
-    cfg.blockDim = dim3(kTkThreads, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -275,19 +411,23 @@ cudaError_t launch_indexer_topk(const TopkArgs& a, cudaStream_t s) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err;
-    if (a.bf16) {
-        err = cudaFuncSetAttribute(indexer_topk_kernel<true>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        err = cudaLaunchKernelEx(&cfg, indexer_topk_kernel<true>, a);
-    } else {
-        err = cudaFuncSetAttribute(indexer_topk_kernel<false>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-        err = cudaLaunchKernelEx(&cfg, indexer_topk_kernel<false>, a);
-    }
+    cudaError_t err = cudaFuncSetAttribute(indexer_topk_kernel<BF16, THREADS, DBITS>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+    if (err != cudaSuccess) return err;
+    err = cudaLaunchKernelEx(&cfg, indexer_topk_kernel<BF16, THREADS, DBITS>, a);
     return err != cudaSuccess ? err : cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_indexer_topk(const TopkArgs& a, cudaStream_t s) {
+    if (a.rows == 0) return cudaSuccess;
+    // short rows (one CTA, few keys): 256 threads and 8-bit digits keep the fixed cost of a
+    // pass small; long rows: 512 threads and 11-bit digits (three passes)
+    const bool shortrow = a.seg <= kShortRow;
+    if (a.bf16)
+        return shortrow ? launch_topk_t<true, 256, 8>(a, s) : launch_topk_t<true, 512, 11>(a, s);
+    return shortrow ? launch_topk_t<false, 256, 8>(a, s) : launch_topk_t<false, 512, 11>(a, s);
 }
 
 }  // namespace moe

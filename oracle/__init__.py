@@ -60,6 +60,8 @@ def _load():
             lib.oracle_router_logits.restype = None
             lib.oracle_dequant_q4.argtypes = [P, P, P, i64, i64, i32, P]
             lib.oracle_dequant_q4.restype = None
+            lib.oracle_dequant.argtypes = [ctypes.c_int, P, P, P, i64, i64, i32, P]
+            lib.oracle_dequant.restype = None
             lib.oracle_moe_layer_rows.argtypes = (
                 [P, i64, i32, i32, i32, i32, P, P, i32, i32] + [P] * 9 + [i32] + [P] * 9
                 + [P, P, i64, P])
@@ -147,6 +149,20 @@ def dequant_q4(q, scale_f16_bits, bias_f16_bits, cols, group=64):
     return out
 
 
+def dequant(q, scale_f16_bits, bias_f16_bits, cols, bits, group=64):
+    """Affine `bits`-bit rows [rows, cols*bits/32] uint32 -> fp32 [rows, cols] (4 or 8)."""
+    if bits not in (4, 8):
+        raise ValueError("bits must be 4 or 8")
+    lib = _load()
+    qq = _c(q, np.uint32)
+    rows = qq.size // (cols * bits // 32)
+    s = _c(scale_f16_bits, np.uint16)
+    b = _c(bias_f16_bits, np.uint16)
+    out = np.zeros((rows, cols), np.float32)
+    lib.oracle_dequant(bits, _ptr(qq), _ptr(s), _ptr(b), rows, cols, group, _ptr(out))
+    return out
+
+
 def route_softmax(logits, top_k):
     """Softmax route on fp32 logits [..., E]: (inds int32, scores fp32) [..., K], weights
     renormalised over the selected experts (always)."""
@@ -183,10 +199,11 @@ def moe_layer(x_bits, inds, scores, experts, shared=None, rows=None, group=64,
               shared_gate=None):
     """Dense per-token MoE layer; returns fp32 y for the listed token rows.
 
-    x_bits: uint16 bf16 bits [T, d].  experts: dict with 'bits' (16 or 4) and, for 16,
-    'gate','up','down' uint16 bf16 bits ([E,I,d],[E,I,d],[E,d,I]); for 4, 'gate','up','down'
-    uint32 packed plus 'gate_s','gate_b',... fp16 bits.  shared: dict of bf16 bits
-    'gate','up','down' ([I,d],[I,d],[d,I]) or None.
+    x_bits: uint16 bf16 bits [T, d].  experts: dict with 'bits' (16, 8 or 4) and, for 16,
+    'gate','up','down' uint16 bf16 bits ([E,I,d],[E,I,d],[E,d,I]); for 8 / 4, 'gate','up',
+    'down' uint32 packed plus 'gate_s','gate_b',... fp16 bits, and optionally 'group' (the
+    inputs per scale; default `group`).  shared: dict of bf16 bits 'gate','up','down'
+    ([I,d],[I,d],[d,I]) or None.
     """
     lib = _load()
     x = _c(x_bits, np.uint16)
@@ -195,6 +212,7 @@ def moe_layer(x_bits, inds, scores, experts, shared=None, rows=None, group=64,
     sc = _c(scores, np.float32)
     K = ind.shape[1]
     bits = int(experts["bits"])
+    group = int(experts.get("group", group))
     if bits == 16:
         g, u, dn = (_c(experts[k], np.uint16) for k in ("gate", "up", "down"))
         E, I = g.shape[0], g.shape[1]

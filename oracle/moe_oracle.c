@@ -30,7 +30,9 @@
  *   R4 SwiGLU form: FFN(v) = W_down (silu(W_gate v) * (W_up v)), silu(a) = a / (1 + e^-a);
  *   R5 4-bit packing: element j of a row lives in 32-bit word j/8, bits 4*(j%8) .. +3
  *      (low nibble first); group j/64; w = scale * q + bias with fp16 scale and bias;
- *   R6 the permutation lists the pairs p = t*K + k sorted by (expert, p).
+ *   R6 the permutation lists the pairs p = t*K + k sorted by (expert, p);
+ *   R25 8-bit packing: element j of a row lives in 32-bit word j/4, bits 8*(j%4) .. +7 (low
+ *      byte first); groups of 32, 64 or 128 inputs share one fp16 scale and bias.
  */
 #include <math.h>
 #include <stdint.h>
@@ -271,7 +273,9 @@ void oracle_router_logits(const uint16_t* x, int64_t T, int d, const uint16_t* w
 /* ------------------------------------------------------------------------------------ */
 
 /* One weight matrix [rows, cols] of one expert.  bits == 16: w16 holds bf16 [rows, cols].
- * bits == 4: q holds uint32 [rows, cols/8]; scale and bias hold fp16 [rows, cols/group]. */
+ * bits == 4 or 8: q holds uint32 [rows, cols*bits/32] (32/bits codes per word, element j in
+ * bits bits*(j % (32/bits)) .. upward of word j / (32/bits): R5 and, for 8 bits, R25);
+ * scale and bias hold fp16 [rows, cols/group]. */
 typedef struct {
     int bits;
     int group;
@@ -281,27 +285,39 @@ typedef struct {
     const uint16_t* bias;
 } oracle_mat_t;
 
-/* w = scale * q + bias, in fp32, element (r, c) of a 4-bit matrix with `cols` columns. */
-float oracle_q4_element(const uint32_t* q, const uint16_t* scale, const uint16_t* bias,
-                        int64_t r, int64_t c, int64_t cols, int group) {
-    uint32_t word = q[r * (cols / 8) + c / 8];
-    uint32_t nib = (word >> (4 * (c % 8))) & 0xfu;
+/* w = scale * q + bias, in fp32, element (r, c) of a `bits`-bit affine matrix with `cols`
+ * columns ([epic] first paragraph: quantised experts through gather_qmm). */
+float oracle_q_element(int bits, const uint32_t* q, const uint16_t* scale,
+                       const uint16_t* bias, int64_t r, int64_t c, int64_t cols, int group) {
+    const int per = 32 / bits;
+    uint32_t word = q[r * (cols / per) + c / per];
+    uint32_t code = (word >> (bits * (c % per))) & ((1u << bits) - 1u);
     int64_t ng = cols / group;
     float s = oracle_f16_to_f32(scale[r * ng + c / group]);
     float b = oracle_f16_to_f32(bias[r * ng + c / group]);
-    return s * (float)nib + b;
+    return s * (float)code + b;
+}
+
+float oracle_q4_element(const uint32_t* q, const uint16_t* scale, const uint16_t* bias,
+                        int64_t r, int64_t c, int64_t cols, int group) {
+    return oracle_q_element(4, q, scale, bias, r, c, cols, group);
+}
+
+void oracle_dequant(int bits, const uint32_t* q, const uint16_t* scale, const uint16_t* bias,
+                    int64_t rows, int64_t cols, int group, float* out) {
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            out[r * cols + c] = oracle_q_element(bits, q, scale, bias, r, c, cols, group);
 }
 
 void oracle_dequant_q4(const uint32_t* q, const uint16_t* scale, const uint16_t* bias,
                        int64_t rows, int64_t cols, int group, float* out) {
-    for (int64_t r = 0; r < rows; ++r)
-        for (int64_t c = 0; c < cols; ++c)
-            out[r * cols + c] = oracle_q4_element(q, scale, bias, r, c, cols, group);
+    oracle_dequant(4, q, scale, bias, rows, cols, group, out);
 }
 
 static double mat_elem(const oracle_mat_t* m, int64_t r, int64_t c, int64_t cols) {
     if (m->bits == 16) return (double)oracle_bf16_to_f32(m->w16[r * cols + c]);
-    return (double)oracle_q4_element(m->q, m->scale, m->bias, r, c, cols, m->group);
+    return (double)oracle_q_element(m->bits, m->q, m->scale, m->bias, r, c, cols, m->group);
 }
 
 /* Expert FFN on one bf16 vector v[d]:  out = W_down (silu(W_gate v) * (W_up v)).
@@ -332,7 +348,7 @@ static oracle_mat_t expert_slice(const oracle_mat_t* m, int64_t e, int64_t rows,
     if (m->bits == 16) {
         s.w16 = m->w16 + e * rows * cols;
     } else {
-        s.q = m->q + e * rows * (cols / 8);
+        s.q = m->q + e * rows * (cols / (32 / m->bits));
         s.scale = m->scale + e * rows * (cols / m->group);
         s.bias = m->bias + e * rows * (cols / m->group);
     }
@@ -360,6 +376,8 @@ int oracle_moe_layer_rows(const uint16_t* x, int64_t T, int d, int I, int E, int
                           const void* shared_gate,
                           const int64_t* rows, int64_t n_rows, float* y) {
     (void)T;
+    if (bits != 16 && bits != 4 && bits != 8) return -1;
+    if (bits != 16 && (group < 1 || d % group || I % group)) return -1;
     oracle_mat_t g = {bits, group, (const uint16_t*)gate_w, (const uint32_t*)gate_w,
                       (const uint16_t*)gate_s, (const uint16_t*)gate_b};
     oracle_mat_t u = {bits, group, (const uint16_t*)up_w, (const uint32_t*)up_w,

@@ -629,3 +629,79 @@ def test_indexer_topk_order_invariant_nan_and_signed_zero():
     # k = 1 is the argmax, first occurrence on ties
     sc4 = rng.randint(0, 5, size=(50, 30)).astype(np.float32)
     assert np.array_equal(oracle.indexer_topk(sc4, 1)[:, 0], np.argmax(sc4, axis=1))
+
+
+# ------------------------------------------------------------------------------------
+# other quantisation widths and groups: 8-bit codes, groups of 32 / 64 / 128 inputs
+# ------------------------------------------------------------------------------------
+
+def _unpack_bytes(words, cols, bits):
+    """Independent unpacker through numpy's little-endian memory view: for 8 bits the
+    codes are the row's bytes in order; for 4 bits each byte holds two codes, low first."""
+    raw = np.ascontiguousarray(np.asarray(words, np.uint32).astype("<u4")).view(np.uint8)
+    raw = raw.reshape(raw.shape[0], -1)
+    if bits == 8:
+        return raw[:, :cols].astype(np.int64)
+    out = np.empty((raw.shape[0], 2 * raw.shape[1]), np.int64)
+    out[:, 0::2] = raw & 15
+    out[:, 1::2] = raw >> 4
+    return out[:, :cols]
+
+
+def test_q8_byte_order_low_first():
+    q = np.array([[0x03020100, 0x07060504, 0xFFFEFDFC, 0x80807F7F]], np.uint32)
+    one = np.array([[np.float16(1.0).view(np.uint16)]], np.uint16)
+    zero = np.array([[np.float16(0.0).view(np.uint16)]], np.uint16)
+    out = oracle.dequant(q, one, zero, cols=16, bits=8, group=16)
+    assert out[0].tolist() == [0, 1, 2, 3, 4, 5, 6, 7, 252, 253, 254, 255, 127, 127, 128, 128]
+
+
+@pytest.mark.parametrize("bits,group", [(8, 32), (8, 64), (8, 128), (4, 32), (4, 128)])
+def test_dequant_affine_widths_and_groups(bits, group):
+    rng = np.random.RandomState(bits * 1000 + group)
+    rows, cols = 3, 384
+    q = rng.randint(0, 2**32, size=(rows, cols * bits // 32), dtype=np.uint64).astype(np.uint32)
+    s = rng.uniform(0.005, 0.02, size=(rows, cols // group)).astype(np.float16)
+    b = (0.1 * rng.randn(rows, cols // group)).astype(np.float16)
+    got = oracle.dequant(q, s.view(np.uint16), b.view(np.uint16), cols, bits, group)
+    codes = _unpack_bytes(q, cols, bits)
+    sf = np.repeat(s.astype(np.float64), group, axis=1)
+    bf = np.repeat(b.astype(np.float64), group, axis=1)
+    assert np.allclose(got, sf * codes + bf, rtol=1e-6, atol=1e-7)
+    # the neighbouring group's scale would show: groups differ
+    wrong = np.repeat(np.roll(s, 1, axis=1).astype(np.float64), group, axis=1) * codes
+    assert not np.allclose(got, wrong + bf, rtol=1e-3)
+    one = np.full((rows, cols // group), np.float16(1)).view(np.uint16)
+    zero = np.zeros((rows, cols // group), np.uint16)
+    assert np.array_equal(oracle.dequant(q, one, zero, cols, bits, group), codes.astype(np.float32))
+    if bits == 4:  # the 4-bit entry point agrees with the general one
+        assert np.array_equal(oracle.dequant_q4(q, s.view(np.uint16), b.view(np.uint16), cols,
+                                                group), got)
+
+
+@pytest.mark.parametrize("bits,group", [(8, 64), (8, 32), (4, 128)])
+def test_layer_quant_widths_match_numpy_float64(bits, group):
+    T, d, I, E, K = 4, 256, 128, 5, 2
+    g = torch.Generator().manual_seed(bits + group)
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    ex, ref_w = {"bits": bits, "group": group}, {}
+    for k, (r, c) in (("gate", (I, d)), ("up", (I, d)), ("down", (d, I))):
+        q = torch.randint(-2**31, 2**31, (E, r, c * bits // 32), generator=g,
+                          dtype=torch.int64).to(torch.int32).numpy().view(np.uint32)
+        sc = (torch.rand(E, r, c // group, generator=g) * 0.01 + 0.002).half().numpy()
+        bi = (torch.randn(E, r, c // group, generator=g) * 0.05).half().numpy()
+        ex[k], ex[k + "_s"], ex[k + "_b"] = q, sc.view(np.uint16), bi.view(np.uint16)
+        ref_w[k] = [(np.repeat(sc[e].astype(np.float64), group, 1) *
+                     _unpack_bytes(q[e], c, bits)).astype(np.float32).astype(np.float64) +
+                    np.repeat(bi[e].astype(np.float64), group, 1) for e in range(E)]
+    inds = np.stack([np.random.RandomState(t).permutation(E)[:K] for t in range(T)]).astype(np.int32)
+    scores = np.random.RandomState(9).rand(T, K).astype(np.float32)
+    got = oracle.moe_layer(_bits(x), inds, scores, ex, None)
+    xs = _f64(x)
+    ref = np.zeros((T, d))
+    for t in range(T):
+        for kk in range(K):
+            e = inds[t, kk]
+            ref[t] += scores[t, kk] * _np_ffn(xs[t], ref_w["gate"][e], ref_w["up"][e],
+                                             ref_w["down"][e])
+    assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max()
