@@ -142,8 +142,8 @@ def algorithmic(w, counts):
     rows = P + (T if w.shared else 0)
     if w.bits == 16:
         wmat = I * d * 2                     # bytes of one [I, d] bf16 matrix
-    else:
-        wmat = I * d // 2 + 2 * (I * d // 64) * 2
+    else:                                    # codes + fp16 scale and bias per group
+        wmat = I * d * w.bits // 8 + 2 * (I * d // w.group) * 2
     shmat = I * d * 2
     gate_up_w = hit * 2 * wmat + nsh * 2 * shmat
     down_w = hit * wmat + nsh * shmat
@@ -205,6 +205,45 @@ def time_routing(dev, replays=50):
     return {"workload": f"routing_{rows}x{E}", "l2": "16 rotating copies of the logits "
             "(269 MB > L2); launches replayed from a CUDA graph",
             "kernel": "route_kernel<8, false>", **out}
+
+
+def time_indexer(dev, reps=20):
+    """The DSA indexer selection on its decode (64 rows x 131072 positions) and causal
+    prefill (8192 x 8192, with the mask) workloads: launches over rotating score copies
+    whose total exceeds L2, timed with CUDA events on the launch stream."""
+    out = {}
+    peaks = load_peaks()[0]
+    for name, want_mask in (("dsa_decode_B64_N131072", False), ("dsa_prefill_L8192", True)):
+        w = inputs.INDEXER_WORKLOADS[name]
+        sc = inputs.gen_indexer_scores(w, dev, seed=0)
+        ln = inputs.indexer_lengths(w, dev)
+        nbuf = max(2, -(-(160 << 20) // (sc.numel() * 4)))
+        bufs = [sc] + [sc.clone() for _ in range(nbuf - 1)]
+        inds = torch.empty(w.rows, w.k, dtype=torch.int32, device=dev)
+        mask = torch.empty(w.rows, w.n, dtype=torch.uint8, device=dev) if want_mask else None
+        stream = torch.cuda.current_stream(dev)
+        for b in bufs[:3]:
+            binding.indexer_topk(b, w.k, lengths=ln, want_mask=want_mask, inds=inds, mask=mask)
+        torch.cuda.synchronize(dev)
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            binding.indexer_topk(bufs[i % nbuf], w.k, lengths=ln, want_mask=want_mask,
+                                 inds=inds, mask=mask)
+        z.record(stream)
+        torch.cuda.synchronize(dev)
+        us = a.elapsed_time(z) * 1e3 / reps
+        valid = w.rows * w.n if ln is None else int(ln.clamp(max=w.n).long().sum())
+        nbytes = valid * 4 + w.rows * w.k * 4 + (w.rows * w.n if want_mask else 0)
+        out[name] = {"rows": w.rows, "n": w.n, "k": w.k, "causal": w.causal, "mask": want_mask,
+                     "us_per_launch": round(us, 2), "rows_per_s": round(w.rows / (us * 1e-6), 1),
+                     "bytes": nbytes, "launches": reps,
+                     "roofline": roofline("hbm", nbytes / (us * 1e-6), peaks, False)}
+        del bufs, sc
+        torch.cuda.empty_cache()
+    out["kernel"] = "indexer_topk_kernel<false> (fp32 scores)"
+    out["l2"] = "rotating score copies totalling > 160 MB (> L2) between launches"
+    return out
 
 
 def make_layer(w, data):
@@ -441,8 +480,18 @@ def run_ours(args):
         q4["q4_prefill"] = summary(wq2, tq2)
         del dq, dq2
         torch.cuda.empty_cache()
+    if args.q8 and w.d == 7168 and w.E == 256:
+        wq, dq = workload_data("dsv3_q8_T32", dev)
+        tq = time_layer(wq, dq, args.steps, args.warmup, dev)
+        q4["q8_decode"] = summary(wq, tq)
+        wq2, dq2 = workload_data("dsv3_q8_T4096_zipf", dev, base=dq)
+        tq2 = time_layer(wq2, dq2, args.steps, args.warmup, dev)
+        q4["q8_prefill"] = summary(wq2, tq2)
+        del dq, dq2
+        torch.cuda.empty_cache()
 
     routing = time_routing(dev) if w.E == inputs.ROUTING["E"] else None
+    indexer = time_indexer(dev) if args.indexer else None
 
     # aggregate over ranks: tokens of all ranks / max time
     tot = torch.tensor([t["total_ms"], e2e["ms"]], dtype=torch.float64)
@@ -480,6 +529,8 @@ def run_ours(args):
     line.update(q4)
     if routing is not None:
         line["routing"] = routing
+    if indexer is not None:
+        line["indexer_topk"] = indexer
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, data)
     if rank == 0:
@@ -534,6 +585,10 @@ def main():
     ap.add_argument("--workload", default="dsv3_T128", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--prefill", default="dsv3_T8192_zipf")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-q8", dest="q8", action="store_false",
+                    help="skip the affine 8-bit expert workloads")
+    ap.add_argument("--no-indexer", dest="indexer", action="store_false",
+                    help="skip the DSA indexer selection workloads")
     ap.add_argument("--no-q4", dest="q4", action="store_false",
                     help="skip the affine 4-bit expert workloads")
     args = ap.parse_args()

@@ -146,8 +146,9 @@ def route_params(top_k, n_group, topk_group, norm_topk_prob, routed_scaling_fact
 
 
 def expert_weights(w: dict | None):
-    """ExpertWeights from a dict: bits 16 -> gate/up/down bf16; bits 4 -> gate/up/down int32
-    (packed uint32 words) plus gate_s/gate_b/up_s/up_b/down_s/down_b fp16."""
+    """ExpertWeights from a dict: bits 16 -> gate/up/down bf16; bits 8 or 4 -> gate/up/down
+    int32 (packed uint32 words) plus gate_s/gate_b/up_s/up_b/down_s/down_b fp16 and an
+    optional 'group' (inputs per scale: 32, 64 or 128; default 64)."""
     if w is None:
         return None
     bits = int(w.get("bits", 16))
@@ -160,7 +161,9 @@ def expert_weights(w: dict | None):
         _need(w[k], torch.int32, k)
     for k in ("gate_s", "gate_b", "up_s", "up_b", "down_s", "down_b"):
         _need(w[k], torch.float16, k)
-    return ExpertWeights(4, int(w.get("group", 64)), w["gate"].data_ptr(), w["up"].data_ptr(),
+    if bits not in (4, 8):
+        raise ValueError(f"bits = {bits}: expert weights are bf16 (16) or affine 8 / 4-bit")
+    return ExpertWeights(bits, int(w.get("group", 64)), w["gate"].data_ptr(), w["up"].data_ptr(),
                          w["down"].data_ptr(), w["gate_s"].data_ptr(), w["gate_b"].data_ptr(),
                          w["up_s"].data_ptr(), w["up_b"].data_ptr(), w["down_s"].data_ptr(),
                          w["down_b"].data_ptr())

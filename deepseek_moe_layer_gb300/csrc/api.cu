@@ -96,13 +96,15 @@ int check_route_params(int32_t E, const moe_route_params_t* p) {
 
 int check_weights(const moe_expert_weights_t* w, const char* what, int shared) {
     MOE_CHECK(w, "%s weights are NULL", what);
-    MOE_CHECK(w->bits == 16 || w->bits == 4, "%s weights: bits = %d (16 or 4)", what, w->bits);
+    MOE_CHECK(w->bits == 16 || w->bits == 8 || w->bits == 4, "%s weights: bits = %d (16, 8 or 4)",
+              what, w->bits);
     MOE_CHECK(!shared || w->bits == 16, "%s weights must be bf16 (bits 16)", what);
     MOE_CHECK(w->gate && w->up && w->down, "%s weights: gate/up/down pointer is NULL", what);
     MOE_CHECK(aligned(w->gate, 16) && aligned(w->up, 16) && aligned(w->down, 16),
               "%s weights: pointers must be 16-byte aligned", what);
-    if (w->bits == 4) {
-        MOE_CHECK(w->group_size == 64, "%s weights: group_size = %d (only 64)", what, w->group_size);
+    if (w->bits != 16) {
+        MOE_CHECK(w->group_size == 32 || w->group_size == 64 || w->group_size == 128,
+                  "%s weights: group_size = %d (32, 64 or 128)", what, w->group_size);
         MOE_CHECK(w->gate_scale && w->gate_bias && w->up_scale && w->up_bias && w->down_scale &&
                       w->down_bias,
                   "%s weights: 4-bit scale/bias pointer is NULL", what);
@@ -234,7 +236,8 @@ int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_
     g.Kdim = d;
     g.F = I;
     g.ksplit = 1;
-    g.w = {ex->bits, ex->gate, ex->up, ex->gate_scale, ex->gate_bias, ex->up_scale, ex->up_bias};
+    g.w = {ex->bits, ex->gate, ex->up, ex->gate_scale, ex->gate_bias, ex->up_scale, ex->up_bias,
+           ex->group_size};
     if (has_shared) g.ws = {16, sh->gate, sh->up, nullptr, nullptr, nullptr, nullptr};
     g.out = h;
     g.out_ld = I;
@@ -251,7 +254,8 @@ int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_
     dn.shared_act_row0 = P;
     dn.Kdim = I;
     dn.F = d;
-    dn.w = {ex->bits, ex->down, nullptr, ex->down_scale, ex->down_bias, nullptr, nullptr};
+    dn.w = {ex->bits, ex->down, nullptr, ex->down_scale, ex->down_bias, nullptr, nullptr,
+            ex->group_size};
     if (has_shared) dn.ws = {16, sh->down, nullptr, nullptr, nullptr, nullptr, nullptr};
     dn.out = out;
     dn.out_ld = d;

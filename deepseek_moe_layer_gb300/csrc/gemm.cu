@@ -58,8 +58,9 @@ __host__ __device__ constexpr int pow2ceil(int v) {
 
 constexpr int kDequantWarps = 8;  // 4-bit variant: warps turning packed codes into bf16
 
-template <int MODE, int TOKT, bool Q4>
+template <int MODE, int TOKT, int QB>
 struct Cfg {
+    static constexpr bool kQ = QB != 0;                              // affine-quantised weights
     static constexpr bool kSwap = TOKT != 0;
     static constexpr int kTok = kSwap ? TOKT : 128;                  // tokens per tile
     static constexpr int kNW = (kSwap && MODE == kGateUp) ? 2 : 1;   // A weight tiles (swap)
@@ -73,22 +74,23 @@ struct Cfg {
     // dequantised tile never crosses shared memory (which would otherwise carry 8x the HBM
     // bytes: bf16 written, then read back by the tensor core).  An operand stage is then
     // the token rows in shared memory plus kAStageCols TMEM columns of weights.
-    static constexpr bool kTA = Q4 && kSwap;
+    static constexpr bool kTA = kQ && kSwap;
     static constexpr int kAStageCols = kNW * 32;  // 64 bf16 of K = 32 columns per weight tile
     static constexpr int kStageBytes = kTA ? kXBytes : kXBytes + kWBytes;  // smem per stage
-    // 4-bit: packed codes travel in a ring of their own.  A raw slot holds kRawKB k-blocks
-    // of every weight row of the tile (a 128-byte row segment, 128-byte swizzled), so each
-    // HBM access is as long as in the bf16 path and the dequant warps read it without bank
-    // conflicts.  On the TMEM-A path a raw slot also carries one k-block of the bf16 shared
-    // expert (the same bytes: 128-byte rows).
-    static constexpr int kRawKB = 4;
-    static constexpr int kRBytes = Q4 ? kWRows * 32 * kRawKB : 0;
+    // quantised: packed codes travel in a ring of their own.  A raw slot holds kRawKB
+    // k-blocks of every weight row of the tile (a 128-byte row segment, 128-byte swizzled:
+    // 4 k-blocks of 4-bit codes or 2 of 8-bit codes), so each HBM access is as long as in
+    // the bf16 path and the dequant warps read it without bank conflicts.  On the TMEM-A
+    // path a raw slot also carries one k-block of the bf16 shared expert (the same bytes:
+    // 128-byte rows).
+    static constexpr int kRawKB = QB == 8 ? 2 : 4;
+    static constexpr int kRBytes = kQ ? kWRows * 128 : 0;
     static constexpr int kStages =
         kTA ? cmin(8, (512 - 2 * kAccCols) / kAStageCols)
-            : cmin(12, (216 * 1024 - (Q4 ? 2 * kRBytes : 0)) / kStageBytes);
+            : cmin(12, (216 * 1024 - (kQ ? 2 * kRBytes : 0)) / kStageBytes);
     static constexpr int kRawStages =
-        !Q4 ? 0 : kTA ? cmin(8, (216 * 1024 - kStages * kStageBytes) / kRBytes) : 2;
-    static constexpr int kThreadsCta = Q4 ? kThreads + 32 + 32 * kDequantWarps : kThreads;
+        !kQ ? 0 : kTA ? cmin(8, (216 * 1024 - kStages * kStageBytes) / kRBytes) : 2;
+    static constexpr int kThreadsCta = kQ ? kThreads + 32 + 32 * kDequantWarps : kThreads;
     static constexpr int kTmemCols = kTA ? 512 : pow2ceil(cmax(32, 2 * kAccCols));
     static constexpr int kN = kSwap ? kTok : 256;
     static constexpr uint32_t kIdesc = idesc_bf16(128, kN);
@@ -106,7 +108,8 @@ struct Cfg {
     static_assert(kN % 16 == 0 && kN >= 16 && kN <= 256, "UMMA N for M = 128");
     static_assert(!kTA || (kStages >= 2 && 2 * kAccCols + kStages * kAStageCols <= 512),
                   "TMEM budget of the TMEM-A path");
-    static_assert(!Q4 || kRawStages >= 2, "raw ring depth");
+    static_assert(!kQ || kRawStages >= 2, "raw ring depth");
+    static_assert(QB == 0 || QB == 4 || QB == 8, "code width");
 };
 
 struct KParams {
@@ -123,10 +126,12 @@ struct KParams {
     long long split_stride;
     void* out;
     long long out_ld;
-    // 4-bit weights: fp16 scale / bias per group of 64 inputs, [rows_total, Kdim / 64]
+    // quantised weights: fp16 scale / bias per group of qgroup inputs, [rows_total,
+    // Kdim / qgroup]
     const unsigned short* qscale[2];
     const unsigned short* qbias[2];
-    int q_vec;  // 8 | Kdim/64 and 16-byte aligned scale/bias arrays: 16-byte group loads
+    int qgroup;  // 32, 64 or 128 (the kernel's QG)
+    int q_vec;   // 8 | Kdim/qgroup and 16-byte aligned scale/bias arrays: 16-byte loads
 };
 
 // Eight packed 4-bit codes (element j in bits 4j..4j+3 of the word) -> eight bf16 weights
@@ -150,6 +155,24 @@ MOE_DEV uint4 dequant8(uint32_t w, uint32_t s2, uint32_t b2) {
         asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(v[i]), "r"(0x43004300u));
         asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r[i]) : "r"(q), "r"(s2), "r"(b2));
     }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Eight packed 8-bit codes (element j in bits 8j..8j+7 of w0 for j < 4, of w1 for j >= 4)
+// -> eight bf16 weights w = scale * q + bias.  Each code becomes the fp32 number 2^23 + q
+// exactly (0x4B exponent byte over the code), 2^23 is subtracted exactly, one fp32 fused
+// multiply-add applies scale and bias, and the pair is rounded once to bf16x2.
+MOE_DEV uint4 dequant8_u8(uint32_t w0, uint32_t w1, float sc, float bi) {
+    float q[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        q[e] = __uint_as_float(__byte_perm(w0, 0x4B000000u, 0x7440u | (uint32_t)e)) - 8388608.0f;
+        q[4 + e] = __uint_as_float(__byte_perm(w1, 0x4B000000u, 0x7440u | (uint32_t)e)) - 8388608.0f;
+    }
+    uint32_t r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        r[i] = pack_bf16x2(fmaf(sc, q[2 * i], bi), fmaf(sc, q[2 * i + 1], bi));
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
@@ -224,15 +247,16 @@ MOE_DEV void record_timeout(volatile int* abort) {
 
 // tm_w0 / tm_w1: bf16 weight rows (Q4 = false) or packed 4-bit code rows (Q4 = true); the
 // shared expert's maps tm_sw0 / tm_sw1 are always bf16.
-template <int MODE, int TOKT, bool Q4>
-__global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
+template <int MODE, int TOKT, int QB, int QG>
+__global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
                     const __grid_constant__ CUtensorMap tm_act_sh,
                     const __grid_constant__ CUtensorMap tm_w0,
                     const __grid_constant__ CUtensorMap tm_w1,
                     const __grid_constant__ CUtensorMap tm_sw0,
                     const __grid_constant__ CUtensorMap tm_sw1, const KParams p) {
-    using C = Cfg<MODE, TOKT, Q4>;
+    using C = Cfg<MODE, TOKT, QB>;
+    constexpr bool Q4 = C::kQ;  // any affine-quantised width (4 or 8 bits)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -384,12 +408,12 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
                     if (!mbar_wait(&rawempty[rs], rph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
                     uint8_t* rst = smem + C::kRawOff + rs * C::kRBytes;
                     mbar_arrive_expect_tx(&rawfull[rs], C::kRBytes);
+                    const int wx = kb * 2 * QB;  // first code word of k-block kb
                     if (MODE == kGateUp) {
-                        tma_load_2d(rst, &tm_w0, &rawfull[rs], kb * 8, wrow, pol_w);
-                        tma_load_2d(rst + 128 * 32 * C::kRawKB, &tm_w1, &rawfull[rs], kb * 8, wrow,
-                                    pol_w);
+                        tma_load_2d(rst, &tm_w0, &rawfull[rs], wx, wrow, pol_w);
+                        tma_load_2d(rst + 128 * 128, &tm_w1, &rawfull[rs], wx, wrow, pol_w);
                     } else {
-                        tma_load_2d(rst, &tm_w0, &rawfull[rs], kb * 8, wrow, pol_w);
+                        tma_load_2d(rst, &tm_w0, &rawfull[rs], wx, wrow, pol_w);
                     }
                 }
             }
@@ -460,7 +484,10 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
         // On the TMEM-A path a warp may only write its own TMEM lane quarter, so the row
         // follows the warp: quarter q = warp % 4, lane -> row q*32 + lane; the two warps of a
         // quarter take the gate and the up tile (gate/up) or the two halves of a row (down).
-        constexpr int kWordsPT = C::kWRows * 8 / (32 * kDequantWarps);
+        constexpr int kWordsPT = C::kWRows * 8 / (32 * kDequantWarps);  // 8-code chunks
+        constexpr int kWPC = QB >= 4 ? QB / 4 : 1;   // code words per chunk (1 or 2)
+        constexpr int kPieces = kWordsPT * kWPC / 4;  // 16-byte pieces of codes per k-block
+        static_assert(!Q4 || kPieces >= 1, "whole 16-byte pieces of codes per thread");
         const int dt = threadIdx.x - kThreads - 32;
         const int qtr = warp & 3;
         const int half = dt / (32 * kDequantWarps / 2);
@@ -472,61 +499,66 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
         const int rr = (MODE == kGateUp) ? (r & 127) : r;
         const unsigned short* sp = mat ? p.qscale[1] : p.qscale[0];
         const unsigned short* bp = mat ? p.qbias[1] : p.qbias[0];
-        const int kgroups = p.Kdim / kBK;
-        // scale/bias of a row are contiguous over its groups: with 8 | kgroups (and 16-byte
-        // aligned arrays) they arrive 8 groups per 16-byte load, one chunk ahead of use;
-        // otherwise one group ahead.  Either way the global latency hides behind dequant work.
+        constexpr int qsh = QG == 32 ? 5 : (QG == 128 ? 7 : 6);  // log2 inputs per group
+        const int ngr = p.Kdim >> qsh;  // scale groups per row
+        // scale/bias of a row are contiguous over its groups: with 8 | ngr (and 16-byte
+        // aligned arrays) they arrive 8 groups per 16-byte load into a sliding window of two
+        // loads (the next one in flight while the current is used); otherwise per k-block.
         const bool vec = p.q_vec != 0;
+        auto pick16 = [](const uint4& v, int j) -> unsigned short {
+            const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
+            return (unsigned short)((j & 1) ? (w >> 16) : (w & 0xFFFFu));
+        };
         int it = 0, rit = 0;  // operand-ring and raw-ring positions
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
             const bool rvalid = !ti.shared && ti.f * C::kFeat + rr < p.F;
             const long long grow = (long long)ti.g * p.F + ti.f * C::kFeat + rr;
-            const unsigned short* srow = sp + grow * kgroups;
-            const unsigned short* brow = bp + grow * kgroups;
+            const unsigned short* srow = sp + grow * ngr;
+            const unsigned short* brow = bp + grow * ngr;
             uint4 sc_cur = make_uint4(0, 0, 0, 0), bc_cur = sc_cur, sc_nxt = sc_cur, bc_nxt = sc_cur;
-            unsigned short s_nxt = 0, b_nxt = 0;
-            if (rvalid) {
-                if (vec) {
-                    sc_cur = __ldg(reinterpret_cast<const uint4*>(srow + ti.kb0));
-                    bc_cur = __ldg(reinterpret_cast<const uint4*>(brow + ti.kb0));
-                    if (ti.kb0 + 8 < kgroups) {
-                        sc_nxt = __ldg(reinterpret_cast<const uint4*>(srow + ti.kb0 + 8));
-                        bc_nxt = __ldg(reinterpret_cast<const uint4*>(brow + ti.kb0 + 8));
-                    }
-                } else {
-                    s_nxt = __ldg(srow + ti.kb0);
-                    b_nxt = __ldg(brow + ti.kb0);
+            int wb = ((ti.kb0 * kBK) >> qsh) & ~7;  // first group of the window (multiple of 8)
+            if (rvalid && vec) {
+                sc_cur = __ldg(reinterpret_cast<const uint4*>(srow + wb));
+                bc_cur = __ldg(reinterpret_cast<const uint4*>(brow + wb));
+                if (wb + 8 < ngr) {
+                    sc_nxt = __ldg(reinterpret_cast<const uint4*>(srow + wb + 8));
+                    bc_nxt = __ldg(reinterpret_cast<const uint4*>(brow + wb + 8));
                 }
             }
             for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++it) {
                 const int s = it % C::kStages;
                 const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
-                unsigned short sb = 0, bb = 0;  // fp16 bits of this row's scale and bias
+                // the (at most two) groups of this thread's chunks in k-block kb
+                const int e0 = kb * kBK + 8 * wd0;
+                const int ga = e0 >> qsh, gb = (e0 + 8 * kWordsPT - 1) >> qsh;
+                unsigned short sa = 0, ba = 0, sb = 0, bb = 0;  // fp16 bits
                 if (vec) {
-                    const int j = (kb - ti.kb0) & 7;
-                    if (j == 0 && kb > ti.kb0) {
+                    if (ga >= wb + 8) {  // the groups advance by at most 2 per k-block
                         sc_cur = sc_nxt;
                         bc_cur = bc_nxt;
-                        if (rvalid && kb + 8 < kgroups) {
-                            sc_nxt = __ldg(reinterpret_cast<const uint4*>(srow + kb + 8));
-                            bc_nxt = __ldg(reinterpret_cast<const uint4*>(brow + kb + 8));
+                        wb += 8;
+                        if (rvalid && wb + 8 < ngr) {
+                            sc_nxt = __ldg(reinterpret_cast<const uint4*>(srow + wb + 8));
+                            bc_nxt = __ldg(reinterpret_cast<const uint4*>(brow + wb + 8));
                         }
                     }
-                    const uint32_t sw = j < 2 ? sc_cur.x : j < 4 ? sc_cur.y : j < 6 ? sc_cur.z : sc_cur.w;
-                    const uint32_t bw = j < 2 ? bc_cur.x : j < 4 ? bc_cur.y : j < 6 ? bc_cur.z : bc_cur.w;
-                    sb = (unsigned short)((j & 1) ? (sw >> 16) : (sw & 0xFFFFu));
-                    bb = (unsigned short)((j & 1) ? (bw >> 16) : (bw & 0xFFFFu));
-                } else {
-                    sb = s_nxt;
-                    bb = b_nxt;
-                    if (rvalid && kb + 1 < ti.kb1) {
-                        s_nxt = __ldg(srow + kb + 1);
-                        b_nxt = __ldg(brow + kb + 1);
-                    }
+                    // both groups lie in the current window: windows start at multiples of
+                    // 8 groups and a split pair is (2m, 2m + 1) for 32-input groups.  The
+                    // next window (still in flight) is only read at the slide above.
+                    const int ia = ga - wb, ib = gb - wb;
+                    sa = pick16(sc_cur, ia);
+                    ba = pick16(bc_cur, ia);
+                    sb = pick16(sc_cur, ib);
+                    bb = pick16(bc_cur, ib);
+                } else if (rvalid) {
+                    sa = __ldg(srow + ga);
+                    ba = __ldg(brow + ga);
+                    sb = __ldg(srow + gb);
+                    bb = __ldg(brow + gb);
                 }
-                uint32_t words[kWordsPT];
+                uint32_t words[kWordsPT * kWPC];
                 if (!ti.shared) {
                     // this row's codes of k-block kb from the current raw slot (a 128-byte
                     // swizzled row segment of kRawKB k-blocks); the slot goes back to the
@@ -539,8 +571,10 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
                     }
                     const uint8_t* rrow = smem + C::kRawOff + rs * C::kRBytes + r * 128;
 #pragma unroll
-                    for (int v = 0; v < kWordsPT / 4; ++v) {
-                        const int c16 = 2 * j + (wd0 + 4 * v) / 4;  // 16-byte chunk in the row
+                    for (int v = 0; v < kPieces; ++v) {
+                        // k-block j starts at byte 8 * QB * j of the row segment, chunk c at
+                        // byte QB * c of the k-block
+                        const int c16 = j * QB / 2 + wd0 * QB / 16 + v;
                         const uint4 q4 =
                             *reinterpret_cast<const uint4*>(rrow + ((c16 ^ (r & 7)) << 4));
                         words[4 * v] = q4.x; words[4 * v + 1] = q4.y;
@@ -590,11 +624,26 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, Q4>::kThreadsCta, 1)
                 // operand slot (free once the MMA has consumed its previous contents)
                 uint4 dq8[kWordsPT];
                 if (!ti.shared) {
-                    const float sf = __half2float(__ushort_as_half(sb));
-                    const float bf = __half2float(__ushort_as_half(bb));
-                    const uint32_t s2 = pack_bf16x2(sf, sf), b2 = pack_bf16x2(bf, bf);
+                    const float sfa = __half2float(__ushort_as_half(sa));
+                    const float bfa = __half2float(__ushort_as_half(ba));
+                    if constexpr (QG != 32) {  // one group for all of this thread's chunks
+                        const uint32_t s2 = pack_bf16x2(sfa, sfa), b2 = pack_bf16x2(bfa, bfa);
 #pragma unroll
-                    for (int w = 0; w < kWordsPT; ++w) dq8[w] = dequant8(words[w], s2, b2);
+                        for (int w = 0; w < kWordsPT; ++w)
+                            dq8[w] = QB == 4 ? dequant8(words[w], s2, b2)
+                                             : dequant8_u8(words[2 * w], words[2 * w + 1], sfa, bfa);
+                    } else {  // 32-input groups: chunk c of a k-block is in its group c / 4
+                        const float sfb = __half2float(__ushort_as_half(sb));
+                        const float bfb = __half2float(__ushort_as_half(bb));
+#pragma unroll
+                        for (int w = 0; w < kWordsPT; ++w) {
+                            const bool second = ((wd0 + w) >> 2) != (wd0 >> 2);
+                            const float sf = second ? sfb : sfa, bf = second ? bfb : bfa;
+                            dq8[w] = QB == 4 ? dequant8(words[w], pack_bf16x2(sf, sf),
+                                                        pack_bf16x2(bf, bf))
+                                             : dequant8_u8(words[2 * w], words[2 * w + 1], sf, bf);
+                        }
+                    }
                 }
                 if (!mbar_wait(&empty[s], ph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
                 if (C::kTA) {
@@ -792,8 +841,8 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D uint32 tensor [rows, cols_u32] of packed 4-bit codes, box of 32 words (4 groups of
-// 64 codes = one 128-byte row segment) x box_rows rows, 128-byte swizzle.
+// 2-D uint32 tensor [rows, cols_u32] of packed codes, box of 32 words (one 128-byte row
+// segment: 256 4-bit or 128 8-bit codes) x box_rows rows, 128-byte swizzle.
 bool make_map_q4(CUtensorMap* m, const void* base, long long rows, long long cols_u32,
                  int box_rows) {
     EncodeTiledFn enc = encode_fn();
@@ -809,13 +858,14 @@ bool make_map_q4(CUtensorMap* m, const void* base, long long rows, long long col
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int TOKT, bool Q4>
+template <int MODE, int TOKT, int QB, int QG>
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
-    using C = Cfg<MODE, TOKT, Q4>;
+    using C = Cfg<MODE, TOKT, QB>;
+    constexpr bool Q4 = C::kQ;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, TOKT, Q4>,
+        attr_err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, TOKT, QB, QG>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::kSmemBytes);
     });
@@ -829,8 +879,9 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
                         a.act_shared ? (a.shared_act_row0 + a.shared_rows) : a.act_rows, a.Kdim,
                         C::kTok);
     if (Q4) {
-        ok = ok && make_map_q4(&m_w0, a.w.w0, wrows_routed, a.Kdim / 8, wbox);
-        ok = ok && make_map_q4(&m_w1, a.w.w1 ? a.w.w1 : a.w.w0, wrows_routed, a.Kdim / 8, wbox);
+        const long long words = (long long)a.Kdim * QB / 32;  // uint32 words of codes per row
+        ok = ok && make_map_q4(&m_w0, a.w.w0, wrows_routed, words, wbox);
+        ok = ok && make_map_q4(&m_w1, a.w.w1 ? a.w.w1 : a.w.w0, wrows_routed, words, wbox);
     } else {
         ok = ok && make_map(&m_w0, a.w.w0, wrows_routed, a.Kdim, wbox);
         ok = ok && make_map(&m_w1, a.w.w1 ? a.w.w1 : a.w.w0, wrows_routed, a.Kdim, wbox);
@@ -862,26 +913,34 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
     p.qscale[1] = static_cast<const unsigned short*>(a.w.s1);
     p.qbias[1] = static_cast<const unsigned short*>(a.w.b1);
     auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
-    p.q_vec = Q4 && (a.Kdim / kBK) % 8 == 0 && a.ksplit == 1 && al16(a.w.s0) && al16(a.w.b0) &&
+    p.qgroup = Q4 ? a.w.group : kBK;
+    p.q_vec = Q4 && (a.Kdim / p.qgroup) % 8 == 0 && al16(a.w.s0) && al16(a.w.b0) &&
               (MODE != kGateUp || (al16(a.w.s1) && al16(a.w.b1)));
 
     long long grid = num_sms();
     if (a.max_tiles < grid) grid = a.max_tiles;
     if (grid < 1) return cudaSuccess;
-    moe_gemm_kernel<MODE, TOKT, Q4><<<(unsigned)grid, C::kThreadsCta, C::kSmemBytes, s>>>(
+    moe_gemm_kernel<MODE, TOKT, QB, QG><<<(unsigned)grid, C::kThreadsCta, C::kSmemBytes, s>>>(
         m_act, m_act_sh, m_w0, m_w1, m_sw0, m_sw1, p);
     return cudaGetLastError();
 }
 
-template <int MODE, bool Q4>
+// Token tiles: the router takes 16 / 32 / 64 / 128 tokens on N or 128 on M; the expert
+// GEMMs take 64 / 128 tokens on N or 128 on M (128 on N bf16 only: the quantised TMEM-A path
+// has no TMEM room for it).
+template <int MODE, int QB, int QG>
 cudaError_t dispatch_tok(const GemmArgs& a, cudaStream_t s) {
     switch (a.tok_tile) {
-        case 0: return run_gemm<MODE, 0, Q4>(a, s);
-        case 16: return run_gemm<MODE, 16, Q4>(a, s);
-        case 32: return run_gemm<MODE, 32, Q4>(a, s);
-        case 64: return run_gemm<MODE, 64, Q4>(a, s);
-        case 128:  // the 4-bit TMEM-A path has no TMEM room for 128-token tiles
-            if constexpr (!Q4) return run_gemm<MODE, 128, Q4>(a, s);
+        case 0: return run_gemm<MODE, 0, QB, QG>(a, s);
+        case 16:
+            if constexpr (MODE == kRouter) return run_gemm<MODE, 16, QB, QG>(a, s);
+            return cudaErrorInvalidValue;
+        case 32:
+            if constexpr (MODE == kRouter) return run_gemm<MODE, 32, QB, QG>(a, s);
+            return cudaErrorInvalidValue;
+        case 64: return run_gemm<MODE, 64, QB, QG>(a, s);
+        case 128:
+            if constexpr (QB == 0) return run_gemm<MODE, 128, QB, QG>(a, s);
             return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
@@ -890,19 +949,28 @@ cudaError_t dispatch_tok(const GemmArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
-    if (a.w.bits == 4) {
+    if (a.w.bits == 4 || a.w.bits == 8) {
         if (a.ws.bits != 16 && a.has_shared) return cudaErrorInvalidValue;
-        switch (a.mode) {
-            case kGateUp: return dispatch_tok<kGateUp, true>(a, s);
-            case kDown: return dispatch_tok<kDown, true>(a, s);
-            default: return cudaErrorInvalidValue;  // the router is always bf16
+        if (a.w.group != 32 && a.w.group != 64 && a.w.group != 128) return cudaErrorInvalidValue;
+        if (a.mode == kRouter) return cudaErrorInvalidValue;  // the router is always bf16
+        const bool gu = a.mode == kGateUp;
+#define MOE_Q_DISPATCH(QB, QG) \
+    return gu ? dispatch_tok<kGateUp, QB, QG>(a, s) : dispatch_tok<kDown, QB, QG>(a, s)
+        if (a.w.bits == 4) {
+            if (a.w.group == 32) MOE_Q_DISPATCH(4, 32);
+            if (a.w.group == 128) MOE_Q_DISPATCH(4, 128);
+            MOE_Q_DISPATCH(4, 64);
         }
+        if (a.w.group == 32) MOE_Q_DISPATCH(8, 32);
+        if (a.w.group == 128) MOE_Q_DISPATCH(8, 128);
+        MOE_Q_DISPATCH(8, 64);
+#undef MOE_Q_DISPATCH
     }
     if (a.w.bits != 16) return cudaErrorInvalidValue;
     switch (a.mode) {
-        case kGateUp: return dispatch_tok<kGateUp, false>(a, s);
-        case kDown: return dispatch_tok<kDown, false>(a, s);
-        case kRouter: return dispatch_tok<kRouter, false>(a, s);
+        case kGateUp: return dispatch_tok<kGateUp, 0, 0>(a, s);
+        case kDown: return dispatch_tok<kDown, 0, 0>(a, s);
+        case kRouter: return dispatch_tok<kRouter, 0, 0>(a, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -71,12 +71,13 @@ cudaError_t launch_indexer_topk(const TopkArgs& a, cudaStream_t s);
 // ---- expert GEMMs (tcgen05) ---------------------------------------------------------
 enum GemmMode { kGateUp = 0, kDown = 1, kRouter = 2 };
 
-struct GemmWeights {             // one stacked weight tensor set (bf16 or affine 4-bit)
-    int bits;
+struct GemmWeights {             // one stacked weight tensor set (bf16 or affine 4/8-bit)
+    int bits;                    // 16, 8 or 4
     const void* w0;              // gate (kGateUp) / down (kDown) / router (kRouter)
     const void* w1;              // up (kGateUp only)
-    const void* s0; const void* b0;   // 4-bit scale / bias of w0
-    const void* s1; const void* b1;   // 4-bit scale / bias of w1
+    const void* s0; const void* b0;   // quantised: fp16 scale / bias of w0
+    const void* s1; const void* b1;   // quantised: fp16 scale / bias of w1
+    int group;                   // quantised: inputs per scale (32, 64 or 128)
 };
 
 struct GemmArgs {

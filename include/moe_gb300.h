@@ -65,11 +65,17 @@ typedef struct {
  * experts, NE = 1 for the shared expert).
  *   bits == 16: gate, up: bf16 [NE, I, d]; down: bf16 [NE, d, I]; the scale/bias
  *               pointers are ignored.
- *   bits == 4 : affine 4-bit, group_size 64 along the input dimension.  gate, up: uint32
- *               [NE, I, d/8]; down: uint32 [NE, d, I/8]; element j of a row is nibble
- *               j%8 (bits 4*(j%8)..+3, low nibble first) of word j/8; *_scale, *_bias:
- *               fp16 [NE, I, d/64] (gate, up) and [NE, d, I/64] (down);
- *               w = scale * q + bias.  All pointers 16-byte aligned.
+ *   bits == 4 : affine 4-bit, one fp16 scale and bias per group_size (32, 64 or 128)
+ *               consecutive inputs.  gate, up: uint32 [NE, I, d/8]; down: uint32
+ *               [NE, d, I/8]; element j of a row is nibble j%8 (bits 4*(j%8)..+3, low
+ *               nibble first) of word j/8; *_scale, *_bias: fp16 [NE, I, d/group_size]
+ *               (gate, up) and [NE, d, I/group_size] (down); w = scale * q + bias.
+ *   bits == 8 : affine 8-bit, the same groups; gate, up: uint32 [NE, I, d/4]; down: uint32
+ *               [NE, d, I/4]; element j of a row is byte j%4 (bits 8*(j%4)..+7, low byte
+ *               first) of word j/4.
+ *   Quantised weights are dequantised to bf16 inside the expert GEMMs (4-bit: one bf16
+ *   fused multiply-add; 8-bit: fp32 fused multiply-add, then one rounding to bf16).
+ *   All pointers 16-byte aligned (the scales and biases: 2-byte).
  */
 typedef struct {
     int32_t bits;
@@ -191,8 +197,9 @@ int moe_router_logits(const void* x, int64_t T, int32_t d, const void* w_router,
  *   ws: device workspace of at least moe_grouped_swiglu_workspace_bytes() bytes,
  *   256-byte aligned; its contents need no initialisation and are clobbered.
  * Errors: MOE_ERR_INVALID for NULL pointers, T < 0, K < 1, E < 1 or > 1024, d or I not a
- * multiple of 128, T*K >= 2^31, bits not 16 or 4, group_size != 64 for bits 4, shared
- * bits != 16, misaligned pointers, or a workspace that is too small.
+ * multiple of 128, T*K >= 2^31, bits not 16, 8 or 4, group_size not 32, 64 or 128 for
+ * quantised weights, shared bits != 16, misaligned pointers, or a workspace that is too
+ * small.
  */
 int moe_grouped_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_t K,
                        const int32_t* offsets, const int32_t* perm,

@@ -74,7 +74,7 @@ def oracle_experts(data_experts, uniq=None):
     sel = (lambda t: t) if uniq is None else (lambda t: t.index_select(0, uniq))
     if ex["bits"] == 16:
         return {"bits": 16, **{k: bits(sel(ex[k])) for k in ("gate", "up", "down")}}
-    o = {"bits": 4}
+    o = {"bits": ex["bits"], "group": ex.get("group", 64)}
     for k in ("gate", "up", "down"):
         o[k] = sel(ex[k]).cpu().numpy().view(np.uint32)
         o[k + "_s"] = bits(sel(ex[k + "_s"]))

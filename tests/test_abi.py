@@ -100,8 +100,9 @@ def _forward(T=4, d=256, I=128, E=16, bits=16, group=64, ws_bytes=None, shared=T
     (dict(d=200), "d = 200"),
     (dict(I=100), "I = 100"),
     (dict(T=-1), "T = -1"),
-    (dict(bits=8), "bits = 8"),
-    (dict(bits=4, group=32), "group_size = 32"),
+    (dict(bits=2), "bits = 2"),
+    (dict(bits=4, group=16), "group_size = 16"),
+    (dict(bits=8, group=256), "group_size = 256"),
     (dict(ws_bytes=1024), "ws_bytes"),
     (dict(top_k=0), "top_k"),
     (dict(n_group=16, topk_group=1), "expert(s) per group"),

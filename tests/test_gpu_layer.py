@@ -270,6 +270,53 @@ def test_q4_dequant_is_exact_for_integer_affine():
 
 
 # ------------------------------------------------------------------------------------
+# affine 8-bit experts and other group sizes (same quantised bar)
+# ------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T", [64, 5, 33, 96, 300])
+def test_q8_layer_token_tiles(T):
+    w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=T, bits=8)
+    r = _check_forward(w, inputs.gen_layer(w, DEV, seed=40 + T))
+    print(T, r["max"], r["mean"])
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("group", [32, 128])
+@pytest.mark.parametrize("T", [33, 300])
+def test_quant_group_sizes(bits, group, T):
+    # T = 33: tokens on N (weights dequantised into TMEM); T = 300: tokens on M
+    w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=T, bits=bits, group=group)
+    r = _check_forward(w, inputs.gen_layer(w, DEV, seed=bits + group + T))
+    print(bits, group, T, r["max"], r["mean"])
+
+
+@pytest.mark.parametrize("T,d,I,E,K,G,tg,group", [
+    (300, 512, 384, 32, 4, 4, 2, 64),
+    (700, 640, 128, 24, 6, 3, 2, 128),
+    (90, 768, 256, 16, 4, 4, 2, 32),
+])
+def test_q8_layer_multi_tile(T, d, I, E, K, G, tg, group):
+    w = inputs.Workload("mt8", T=T, d=d, E=E, I=I, top_k=K, n_group=G, topk_group=tg,
+                        norm_topk_prob=True, routed_scaling_factor=2.5, bias_var=0.05, bits=8,
+                        group=group)
+    _check_forward(w, inputs.gen_layer(w, DEV, seed=3))
+
+
+def test_q8_dequant_is_exact_for_integer_affine():
+    """scale = 1/256 and bias = -127.5/256: every dequantised weight (q - 127.5)/256 has at
+    most 8 significant bits, exact in bf16, so the 8-bit path must meet the bf16 layer bar."""
+    for T in (40, 300):
+        w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=T, bits=8)
+        data = inputs.gen_layer(w, DEV, seed=6)
+        ex = data["experts"]
+        for k in ("gate", "up", "down"):
+            ex[k + "_s"].fill_(1.0 / 256)
+            ex[k + "_b"].fill_(-127.5 / 256)
+        r = _check_forward(w, data)
+        assert r["max"] < 1e-2 and r["mean"] < 5e-3
+
+
+# ------------------------------------------------------------------------------------
 # DeepSeek-V3-shaped layers at full size, outputs checked on sampled tokens
 # ------------------------------------------------------------------------------------
 
@@ -315,6 +362,30 @@ def test_dsv3_q4_decode_T32(dsv3_q4_weights):
 def test_dsv3_q4_prefill_T4096_zipf(dsv3_q4_weights):
     w = inputs.WORKLOADS["dsv3_q4_T4096_zipf"]
     data = dict(dsv3_q4_weights)
+    data["x"] = inputs.gen_tokens(w, DEV, seed=0)
+    data["logit_offset"] = inputs.zipf_offsets(w.E, DEV, 0)
+    r = _check_forward(w, data, rows=[0, 2048, 4095], check_logits_rows=np.arange(0, 4096, 61))
+    print(r["ties"], r["max"], r["mean"], int((r["counts"] > 0).sum()), int(r["counts"].max()))
+
+
+@pytest.fixture(scope="module")
+def dsv3_q8_weights():
+    w = inputs.WORKLOADS["dsv3_q8_T32"]
+    data = inputs.gen_layer(w, DEV, seed=0)
+    yield data
+    del data
+    torch.cuda.empty_cache()
+
+
+def test_dsv3_q8_decode_T32(dsv3_q8_weights):
+    w = inputs.WORKLOADS["dsv3_q8_T32"]
+    r = _check_forward(w, dsv3_q8_weights, rows=[0, 17, 31])
+    print(r["ties"], r["max"], r["mean"], int((r["counts"] > 0).sum()))
+
+
+def test_dsv3_q8_prefill_T4096_zipf(dsv3_q8_weights):
+    w = inputs.WORKLOADS["dsv3_q8_T4096_zipf"]
+    data = dict(dsv3_q8_weights)
     data["x"] = inputs.gen_tokens(w, DEV, seed=0)
     data["logit_offset"] = inputs.zipf_offsets(w.E, DEV, 0)
     r = _check_forward(w, data, rows=[0, 2048, 4095], check_logits_rows=np.arange(0, 4096, 61))
