@@ -29,6 +29,8 @@ namespace {
 namespace cg = cooperative_groups;
 
 constexpr unsigned kAll = 0xFFFFFFFFu;
+constexpr int kSample = 512;    // keys sampled per row for the threshold window
+constexpr int kCandCap = 4096;  // window keys a CTA can hold
 
 // Order-preserving key of an fp32 score: NaN -> 0 (lowest), -0 -> +0.
 MOE_DEV uint32_t score_key(float f) {
@@ -89,11 +91,10 @@ MOE_DEV uint4 keys4(const uint32_t* keys, int i, int end) {
 }
 
 // THREADS threads per CTA; digits of DBITS bits (the last pass takes the remaining bits).
-template <bool BF16, int THREADS, int DBITS>
+template <bool BF16, int THREADS, int DBITS, bool CACHED>
 __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a) {
     constexpr int W = THREADS / 32;
     constexpr int NB = 1 << DBITS;
-    constexpr int NPASS = (32 + DBITS - 1) / DBITS;
     cg::cluster_group cl = cg::this_cluster();
     const unsigned nc = cl.num_blocks();
     const unsigned rank = cl.block_rank();
@@ -103,11 +104,18 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
     extern __shared__ __align__(16) uint8_t tk_smem[];
     int* hist = reinterpret_cast<int*>(tk_smem);                  // [NB] this CTA's histogram
     int* merged = hist + NB;                                       // [NB] the cluster's sum
-    uint32_t* keys = reinterpret_cast<uint32_t*>(merged + NB);     // [seg] when cached
+    // the threshold window (long rows only): candidates and the sample
+    constexpr bool kWin = THREADS == 512;
+    uint32_t* cand = reinterpret_cast<uint32_t*>(merged + NB);    // [kCandCap] window keys
+    uint32_t* samp = cand + (kWin ? kCandCap : 0);                 // [kSample] (leader's used)
+    uint32_t* keys = samp + (kWin ? kSample : 0);                  // [seg] when cached
     __shared__ uint32_t s_warp[W];
     __shared__ uint32_t s_wg[W], s_wq[W];  // per-warp greater / equal counts, then prefixes
     __shared__ int s_pick[2];               // chosen digit, remaining count
     __shared__ int s_counts[2];             // this CTA's (greater, equal) counts
+    __shared__ int s_wcnt[2];               // keys above / inside the window
+    __shared__ uint32_t s_win[2];           // window (low, high) keys, set by the leader
+    __shared__ int s_ccnt;                  // candidates written
 
     const int n = a.n, k = a.k;
     int nr = a.lengths ? a.lengths[row] : n;
@@ -144,7 +152,7 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
 
     const void* srow = BF16 ? (const void*)(static_cast<const uint16_t*>(a.scores) + row * a.ld)
                             : (const void*)(static_cast<const float*>(a.scores) + row * a.ld);
-    const bool cached = a.cached != 0;
+    constexpr bool cached = CACHED;  // keys of the segment held in shared memory
     if (cached) {
         // one pass over HBM: 16-byte vectors where the row allows, scalars otherwise
         const int per = BF16 ? 8 : 4;
@@ -152,7 +160,41 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
                                (uintptr_t)j0 * (BF16 ? 2u : 4u);
         const bool vec = (addr & 15u) == 0;
         const int nv = vec ? cnt / per : 0;
-        for (int v = tid; v < nv; v += THREADS) {
+        // eight 16-byte loads in flight per thread before any is converted
+        constexpr int kU = 8;
+        int v0 = tid;
+        for (; v0 + (kU - 1) * THREADS < nv; v0 += kU * THREADS) {
+            uint4 qq[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                qq[u] = __ldg(reinterpret_cast<const uint4*>(addr) + v0 + u * THREADS);
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int v = v0 + u * THREADS;
+                const uint32_t w[4] = {qq[u].x, qq[u].y, qq[u].z, qq[u].w};
+                if (BF16) {
+                    uint4 lo, hi;
+                    lo.x = score_key(__uint_as_float(w[0] << 16));
+                    lo.y = score_key(__uint_as_float(w[0] & 0xFFFF0000u));
+                    lo.z = score_key(__uint_as_float(w[1] << 16));
+                    lo.w = score_key(__uint_as_float(w[1] & 0xFFFF0000u));
+                    hi.x = score_key(__uint_as_float(w[2] << 16));
+                    hi.y = score_key(__uint_as_float(w[2] & 0xFFFF0000u));
+                    hi.z = score_key(__uint_as_float(w[3] << 16));
+                    hi.w = score_key(__uint_as_float(w[3] & 0xFFFF0000u));
+                    reinterpret_cast<uint4*>(keys)[2 * v] = lo;
+                    reinterpret_cast<uint4*>(keys)[2 * v + 1] = hi;
+                } else {
+                    uint4 kq;
+                    kq.x = score_key(__uint_as_float(w[0]));
+                    kq.y = score_key(__uint_as_float(w[1]));
+                    kq.z = score_key(__uint_as_float(w[2]));
+                    kq.w = score_key(__uint_as_float(w[3]));
+                    reinterpret_cast<uint4*>(keys)[v] = kq;
+                }
+            }
+        }
+        for (int v = v0; v < nv; v += THREADS) {
             const uint4 q = reinterpret_cast<const uint4*>(addr)[v];
             const uint32_t w[4] = {q.x, q.y, q.z, q.w};
             if (BF16) {
@@ -182,7 +224,7 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
 
     // four keys of this CTA's segment starting at i (a multiple of 4)
     auto get4 = [&](int i) -> uint4 {
-        if (cached) return keys4(keys, i, cnt);
+        if constexpr (CACHED) return keys4(keys, i, cnt);
         uint4 q;
         q.x = i < cnt ? load_key<BF16>(srow, j0 + i) : 0u;
         q.y = i + 1 < cnt ? load_key<BF16>(srow, j0 + i + 1) : 0u;
@@ -195,33 +237,142 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
         else __syncthreads();
     };
 
+    // ---- a window of keys holding the k-th largest, from a sample (cached rows) ----
+    // The leader CTA sorts ~kSample keys taken at a fixed stride of the valid row, takes the
+    // keys delta ranks above and below the k-th largest's expected rank, and the cluster
+    // counts exactly how many keys lie above and inside that window (register counters, no
+    // atomics).  When the k-th largest provably lies inside, only the window's keys (the
+    // candidates) enter the radix select; otherwise every key does.
+    bool windowed = false;
+    uint32_t wlo = 0u, whi = 0xFFFFFFFFu;  // the window (inclusive), when windowed
+    int kk0 = k;               // rank of the threshold among the radix select's keys
+    int ccnt = 0;              // candidates of this CTA
+    uint32_t above_win = 0;    // this CTA's keys above the window
+    if (kWin && cached && (long long)k * 8 <= nr) {  // sparse selections (decode-like rows)
+        const int stride = (nr + kSample - 1) / kSample;
+        const int ns = (nr + stride - 1) / stride;  // <= kSample
+        uint32_t* samp0 = nc > 1 ? cl.map_shared_rank(samp, 0) : samp;
+        for (int j = (j0 + stride - 1) / stride * stride + tid * stride; j < v1; j += THREADS * stride)
+            samp0[j / stride] = keys[j - j0];
+        csync();
+        if (rank == 0) {
+            int n2 = 1;
+            while (n2 < ns) n2 <<= 1;
+            for (int i = ns + tid; i < n2; i += THREADS) samp[i] = 0u;
+            __syncthreads();
+            // bitonic sort, descending
+            for (int size = 2; size <= n2; size <<= 1)
+                for (int st = size >> 1; st > 0; st >>= 1) {
+                    for (int i = tid; i < (n2 >> 1); i += THREADS) {
+                        const int lo = 2 * i - (i & (st - 1)), hi = lo + st;  // st: power of 2
+                        const bool desc = (lo & size) == 0;
+                        const uint32_t x = samp[lo], y = samp[hi];
+                        if ((x < y) == desc) { samp[lo] = y; samp[hi] = x; }
+                    }
+                    __syncthreads();
+                }
+            if (tid == 0) {
+                const int r = (int)((long long)k * ns / nr);
+                const int delta = 3 * (int)sqrtf((float)r) + 8;  // ~3 sigma of the sample rank
+                s_win[0] = r + delta < ns ? samp[r + delta] : 0u;          // low end
+                s_win[1] = r - delta >= 0 ? samp[r - delta] : 0xFFFFFFFFu;  // high end
+            }
+        }
+        csync();
+        const uint32_t* w0p = nc > 1 ? cl.map_shared_rank(s_win, 0) : s_win;
+        wlo = w0p[0];
+        whi = w0p[1];
+        uint32_t a = 0, wn = 0;
+        for (int base = 0; base < cnt; base += 4 * THREADS) {
+            const int i = base + 4 * tid;
+            const uint4 q = keys4(keys, i, cnt);
+            const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool v = i + e < cnt;
+                a += v && kq[e] > whi;
+                wn += v && kq[e] >= wlo && kq[e] <= whi;
+            }
+        }
+        uint32_t ta, tw;
+        block_excl_scan<THREADS>(a, s_warp, &ta);
+        block_excl_scan<THREADS>(wn, s_warp, &tw);
+        if (tid == 0) { s_wcnt[0] = (int)ta; s_wcnt[1] = (int)tw; }
+        csync();
+        long long G = 0, Wt = 0;
+        bool fits = true;
+        for (unsigned c = 0; c < nc; ++c) {
+            const int* rc = c == rank ? s_wcnt : cl.map_shared_rank(s_wcnt, c);
+            G += rc[0];
+            Wt += rc[1];
+            fits = fits && rc[1] <= kCandCap;
+        }
+        csync();  // the counts were read: s_wcnt may be reused
+        windowed = fits && G < k && G + Wt >= k;
+        if (windowed) {
+            kk0 = k - (int)G;
+            above_win = ta;
+            // candidates into shared memory, in any order (warp-aggregated slots)
+            if (tid == 0) s_ccnt = 0;
+            __syncthreads();
+            for (int base = 0; base < cnt; base += 4 * THREADS) {
+                const int i = base + 4 * tid;
+                const uint4 q = keys4(keys, i, cnt);
+                const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool in = i + e < cnt && kq[e] >= wlo && kq[e] <= whi;
+                    const unsigned m = __ballot_sync(kAll, in);
+                    int slot = 0;
+                    if (lane == 0 && m) slot = atomicAdd(&s_ccnt, __popc(m));
+                    slot = __shfl_sync(kAll, slot, 0);
+                    if (in) cand[slot + __popc(m & ((1u << lane) - 1u))] = kq[e];
+                }
+            }
+            __syncthreads();
+            ccnt = s_ccnt;
+        }
+    }
+    // the radix select's keys: the candidates, or every key of the segment
+    auto getr4 = [&](int i) -> uint4 {
+        if constexpr (CACHED) return keys4(windowed ? cand : keys, i, windowed ? ccnt : cnt);
+        return get4(i);
+    };
+    const int rcnt = windowed ? ccnt : cnt;
+
     // ---- radix select of the k-th largest key over the cluster ----
+    // Over the candidates the digits are those of key - wlo, 8 bits at a time, over only the
+    // window's significant bits: small histograms keep the cluster merges cheap.
+    const int dbits = windowed ? 8 : DBITS;
+    const uint32_t kbase = windowed ? wlo : 0u;
+    const int nbits = windowed ? (whi == wlo ? 1 : 32 - __clz((int)(whi - wlo))) : 32;
+    const int npass = (nbits + dbits - 1) / dbits;
     uint32_t prefix = 0, pmask = 0;
-    int kk = k;           // elements still to take among those matching the prefix
+    int kk = kk0;         // elements still to take among those matching the prefix
     uint32_t my_gt = 0;   // this thread's share of the CTA's count of keys above the result
     int last_digit = 0;
 #pragma unroll 1
-    for (int pass = 0; pass < NPASS; ++pass) {
-        const int top = 32 - DBITS * pass;
-        const int shift = top > DBITS ? top - DBITS : 0;
+    for (int pass = 0; pass < npass; ++pass) {
+        const int top = nbits - dbits * pass;
+        const int shift = top > dbits ? top - dbits : 0;
         const int nb = 1 << (top - shift);
         for (int b = tid; b < nb; b += THREADS) hist[b] = 0;
         __syncthreads();
-        for (int base = 0; base < cnt; base += 4 * THREADS) {
+        for (int base = 0; base < rcnt; base += 4 * THREADS) {
             const int i = base + 4 * tid;
-            const uint4 q = get4(i);
+            const uint4 q = getr4(i);
             const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
             bool want[4];
             bool any = false;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                want[e] = i + e < cnt && (kq[e] & pmask) == prefix;
+                want[e] = i + e < rcnt && ((kq[e] - kbase) & pmask) == prefix;
                 any |= want[e];
             }
             if (pass == 0 || __any_sync(kAll, any)) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const uint32_t bin = (kq[e] >> shift) & (uint32_t)(nb - 1);
+                    const uint32_t bin = ((kq[e] - kbase) >> shift) & (uint32_t)(nb - 1);
                     if (want[e]) atomicAdd(&hist[bin], 1);
                 }
             }
@@ -267,13 +418,13 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
         last_digit = d;
         __syncthreads();
     }
-    const uint32_t tau = prefix;  // key of the k-th largest; kk of the keys equal to it are taken
+    const uint32_t tau = prefix + kbase;  // key of the k-th largest; kk of the keys equal to it are taken
 
     // ---- this CTA's counts, its share of the threshold ties and its output base ----
     uint32_t cta_gt;
     block_excl_scan<THREADS>(my_gt, s_warp, &cta_gt);
     if (tid == 0) {
-        s_counts[0] = (int)cta_gt;
+        s_counts[0] = (int)(cta_gt + above_win);
         s_counts[1] = hist[last_digit];  // keys equal to tau in this CTA
     }
     int rem = kk, out_base = 0, take = 0;
@@ -391,12 +542,15 @@ void indexer_topk_plan(TopkArgs& a) {
 }
 
 size_t indexer_topk_smem(int seg, int cached) {
-    const int nb = seg <= kShortRow ? 256 : 2048;
-    return (size_t)2 * nb * sizeof(int) + (cached ? (size_t)seg * sizeof(uint32_t) : 0);
+    const bool shortrow = seg <= kShortRow;
+    const int nb = shortrow ? 256 : 2048;
+    return (size_t)2 * nb * sizeof(int) +
+           (shortrow ? 0 : (size_t)(kCandCap + kSample) * sizeof(uint32_t)) +
+           (cached ? (size_t)seg * sizeof(uint32_t) : 0);
 }
 
 namespace {
-template <bool BF16, int THREADS, int DBITS>
+template <bool BF16, int THREADS, int DBITS, bool CACHED>
 cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
     const size_t smem = indexer_topk_smem(a.seg, a.cached);
     cudaLaunchConfig_t cfg = {};
@@ -411,11 +565,11 @@ cudaError_t launch_topk_t(const TopkArgs& a, cudaStream_t s) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err = cudaFuncSetAttribute(indexer_topk_kernel<BF16, THREADS, DBITS>,
+    cudaError_t err = cudaFuncSetAttribute(indexer_topk_kernel<BF16, THREADS, DBITS, CACHED>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
     if (err != cudaSuccess) return err;
-    err = cudaLaunchKernelEx(&cfg, indexer_topk_kernel<BF16, THREADS, DBITS>, a);
+    err = cudaLaunchKernelEx(&cfg, indexer_topk_kernel<BF16, THREADS, DBITS, CACHED>, a);
     return err != cudaSuccess ? err : cudaGetLastError();
 }
 }  // namespace
@@ -424,10 +578,16 @@ cudaError_t launch_indexer_topk(const TopkArgs& a, cudaStream_t s) {
     if (a.rows == 0) return cudaSuccess;
     // short rows (one CTA, few keys): 256 threads and 8-bit digits keep the fixed cost of a
     // pass small; long rows: 512 threads and 11-bit digits (three passes)
+    // (short rows are always cached: kShortRow <= the 16384-key segment cap)
     const bool shortrow = a.seg <= kShortRow;
-    if (a.bf16)
-        return shortrow ? launch_topk_t<true, 256, 8>(a, s) : launch_topk_t<true, 512, 11>(a, s);
-    return shortrow ? launch_topk_t<false, 256, 8>(a, s) : launch_topk_t<false, 512, 11>(a, s);
+    if (a.bf16) {
+        if (shortrow) return launch_topk_t<true, 256, 8, true>(a, s);
+        return a.cached ? launch_topk_t<true, 512, 11, true>(a, s)
+                        : launch_topk_t<true, 512, 11, false>(a, s);
+    }
+    if (shortrow) return launch_topk_t<false, 256, 8, true>(a, s);
+    return a.cached ? launch_topk_t<false, 512, 11, true>(a, s)
+                    : launch_topk_t<false, 512, 11, false>(a, s);
 }
 
 }  // namespace moe
