@@ -28,16 +28,30 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int k = 0; k < K; ++k) {
-        const int j = inv[t * K + k];
-        if (j < 0) continue;
-        const float w = scores[t * K + k];
-        const uint4 q = __ldg(eo + (long long)j * vec_per_row + v);
-        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+    // K rows in chunks of 4: the chunk's slot ids, then its rows, all in flight together;
+    // the sum still runs k = 0, 1, .., K-1
+    for (int k0 = 0; k0 < K; k0 += 4) {
+        int jj[4];
+        float ww[4];
+        uint4 qq[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc[2 * i] = fmaf(w, bf16_lo(u[i]), acc[2 * i]);
-            acc[2 * i + 1] = fmaf(w, bf16_hi(u[i]), acc[2 * i + 1]);
+        for (int c = 0; c < 4; ++c) {
+            jj[c] = k0 + c < K ? __ldg(inv + t * K + k0 + c) : -1;
+            ww[c] = k0 + c < K ? __ldg(scores + t * K + k0 + c) : 0.0f;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            qq[c] = jj[c] >= 0 ? __ldg(eo + (long long)jj[c] * vec_per_row + v)
+                               : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (jj[c] < 0) continue;
+            const uint32_t u[4] = {qq[c].x, qq[c].y, qq[c].z, qq[c].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(ww[c], bf16_lo(u[i]), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(ww[c], bf16_hi(u[i]), acc[2 * i + 1]);
+            }
         }
     }
     if (so) {

@@ -123,7 +123,17 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     const long long t = perm[j] / K;
     const uint4* src = x + t * vec_per_row;
     uint4* dst = x_perm + j * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    // four 16-byte loads in flight per lane before the stores
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+        const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
+                    e = __ldg(src + v + 96);
+        dst[v] = a;
+        dst[v + 32] = b;
+        dst[v + 64] = c;
+        dst[v + 96] = e;
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
 }
 
 }  // namespace
