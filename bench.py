@@ -134,6 +134,25 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(times, dev=None):
+    """Element-wise maximum of this rank's timings over all ranks (identity without a process
+    group): the slowest replica sets the job's time."""
+    t = torch.tensor([float(v) for v in times], dtype=torch.float64)
+    if torch.distributed.is_available() and torch.distributed.is_initialized() and \
+            torch.distributed.get_world_size() > 1:
+        backend = torch.distributed.get_backend()
+        t = t.to(dev if backend == "nccl" else "cpu")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t = t.cpu()
+    return [float(v) for v in t]
+
+
+def replica_throughput(world_size, steps, tokens_per_step, total_ms):
+    """Whole-job tokens/s of `world_size` replicas, each timing `steps` steps of
+    `tokens_per_step` tokens: all ranks' tokens over the slowest rank's time."""
+    return world_size * steps * tokens_per_step / (total_ms / 1e3)
+
+
 def algorithmic(w, counts):
     """Algorithmic bytes and FLOPs of one forward, from the measured expert loads."""
     T, d, I, E, K = w.T, w.d, w.I, w.E, w.top_k
@@ -499,13 +518,8 @@ def run_ours(args):
     indexer = time_indexer(dev) if args.indexer else None
 
     # aggregate over ranks: tokens of all ranks / max time
-    tot = torch.tensor([t["total_ms"], e2e["ms"]], dtype=torch.float64)
-    if ws > 1:
-        tot = tot.to(dev)
-        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
-        tot = tot.cpu()
-    total_ms, e2e_ms = float(tot[0]), float(tot[1])
-    value = ws * args.steps * w.T / (total_ms / 1e3)
+    total_ms, e2e_ms = max_over_ranks([t["total_ms"], e2e["ms"]], dev)
+    value = replica_throughput(ws, args.steps, w.T, total_ms)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup,
