@@ -22,15 +22,18 @@
  * pages leave open, is evaluated in double on bf16-exact (or dequantised) operands; the
  * intermediate h is not rounded.
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent, named R<n> where the code below applies them:
  *   R1 order within the K selected experts: descending biased score, ties to the lower
  *      expert index (the reference's argpartition leaves the order unspecified);
  *   R2 group-drop ties: among groups of equal group score the lower group index is kept;
  *   R3 NaN is the lowest value in every comparison; -0.0 compares equal to +0.0;
  *   R4 SwiGLU form: FFN(v) = W_down (silu(W_gate v) * (W_up v)), silu(a) = a / (1 + e^-a);
  *   R5 4-bit packing: element j of a row lives in 32-bit word j/8, bits 4*(j%8) .. +3
- *      (low nibble first); group j/64; w = scale * q + bias with fp16 scale and bias;
+ *      (low nibble first); w = scale * q + bias with the fp16 scale and bias of element j's
+ *      group of consecutive inputs (64 unless the weights say 32 or 128);
  *   R6 the permutation lists the pairs p = t*K + k sorted by (expert, p);
+ *   R19 softmax route: the K largest logits are selected (ties as R1) and their weights are
+ *      the softmax over the selected logits only, i.e. always renormalised;
  *   R25 8-bit packing: element j of a row lives in 32-bit word j/4, bits 8*(j%4) .. +7 (low
  *      byte first); groups of 32, 64 or 128 inputs share one fp16 scale and bias.
  */
@@ -436,7 +439,7 @@ int oracle_moe_layer_rows(const uint16_t* x, int64_t T, int d, int I, int E, int
  * causal mask; and the inertness remark: while a row has no more than index_topk positions
  * the selection is every position (dense attention).
  *
- * Readings (listed in the design notes): a row r has n_r valid positions j < n_r (n_r from
+ * Readings where the page is silent: a row r has n_r valid positions j < n_r (n_r from
  * `lengths`, the causal length, or n); the selection is the min(k, n_r) largest valid scores
  * in the order "larger score first, equal scores by lower position" (NaN lowest, -0 == +0),
  * returned as positions in ascending order and padded with -1 up to k; the optional mask
