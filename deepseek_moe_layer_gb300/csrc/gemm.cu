@@ -102,8 +102,13 @@ struct Cfg {
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kPrefixOff = kMiscOff + 16;
     static constexpr int kRowOffOff = kPrefixOff + 4 * (kMaxGroups + 1);
-    static constexpr int kSmemBytes = kRowOffOff + 4 * (kMaxGroups + 1) + 1024;  // + align
+    // bf16 gate/up and down with tokens on M: each epilogue warp stages 32 rows x 64 bf16
+    // (4 KB) so that its global stores cover whole 128-byte lines
+    static constexpr int kEpiOff = (kRowOffOff + 4 * (kMaxGroups + 1) + 127) / 128 * 128;
+    static constexpr int kEpiBytes = (MODE != kRouter && !kSwap && !kQ) ? 4 * 4096 : 0;
+    static constexpr int kSmemBytes = kEpiOff + kEpiBytes + 1024;  // + align
     static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+    static_assert(kEpiOff % 16 == 0, "16-byte shared accesses of the staging buffer");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert(kN % 16 == 0 && kN >= 16 && kN <= 256, "UMMA N for M = 128");
     static_assert(!kTA || (kStages >= 2 && 2 * kAccCols + kStages * kAStageCols <= 512),
@@ -696,7 +701,50 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                 const int r = q * 32 + lane;
                 const bool valid = r < ti.rows;
                 const long long orow = ti.out_row + r;
-                if (MODE == kGateUp) {
+                if (MODE == kGateUp && C::kEpiBytes > 0) {
+                    // h = silu(g) * u, 64 columns per staged chunk (as in the down epilogue)
+                    uint8_t* stg = smem + C::kEpiOff + q * 4096;
+                    const long long row0 = ti.out_row + q * 32;
+                    const int fbase = ti.f * 128;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 128; c0 += 64) {
+#pragma unroll 1
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t g[32], u[32];
+                            __syncwarp();
+                            tmem_ld32(tacc + c0 + 32 * hh, g);
+                            tmem_ld32(tacc + 128 + c0 + 32 * hh, u);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                uint32_t w4[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int c = v * 8 + i * 2;
+                                    w4[i] = pack_bf16x2(
+                                        silu(__uint_as_float(g[c])) * __uint_as_float(u[c]),
+                                        silu(__uint_as_float(g[c + 1])) * __uint_as_float(u[c + 1]));
+                                }
+                                const int j = 4 * hh + v;
+                                *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                            }
+                        }
+                        __syncwarp();
+                        const int j = lane & 7;
+                        const bool cvalid = fbase + c0 + 8 * j + 8 <= p.F;  // F % 8 == 0
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) {
+                            const int rr = it * 4 + (lane >> 3);
+                            const uint4 w =
+                                *reinterpret_cast<const uint4*>(stg + rr * 128 + ((j ^ (rr & 7)) << 4));
+                            if (q * 32 + rr < ti.rows && cvalid)
+                                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16_raw*>(p.out) +
+                                                          (row0 + rr) * p.out_ld + fbase + c0 +
+                                                          8 * j) = w;
+                        }
+                    }
+                } else if (MODE == kGateUp) {
                     __nv_bfloat16_raw* dst = static_cast<__nv_bfloat16_raw*>(p.out) +
                                              orow * p.out_ld + (long long)ti.f * 128;
 #pragma unroll 1
@@ -720,6 +768,43 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                                 }
                                 d4[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                             }
+                        }
+                    }
+                } else if (MODE == kDown && C::kEpiBytes > 0) {
+                    // 64 columns at a time: this warp's 32 rows go to its staging buffer as
+                    // bf16 (16-byte chunk j of row r at chunk j ^ (r % 8): conflict-free), then
+                    // back out with 8 lanes per row, each warp store four whole 128-byte lines
+                    uint8_t* stg = smem + C::kEpiOff + q * 4096;
+                    const int fbase = ti.f * 256;
+                    const long long row0 = ti.out_row + q * 32;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 256 && fbase + c0 < p.F; c0 += 64) {
+                        uint32_t a[32], b[32];
+                        __syncwarp();
+                        tmem_ld32(tacc + c0, a);
+                        tmem_ld32(tacc + c0 + 32, b);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t* v = j < 4 ? a + 8 * j : b + 8 * (j - 4);
+                            *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                                make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                                           pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                                           pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                                           pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
+                        }
+                        __syncwarp();
+                        const int j = lane & 7;
+                        const bool cvalid = fbase + c0 + 8 * j + 8 <= p.F;  // F % 8 == 0
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) {
+                            const int rr = it * 4 + (lane >> 3);
+                            const uint4 w =
+                                *reinterpret_cast<const uint4*>(stg + rr * 128 + ((j ^ (rr & 7)) << 4));
+                            if (q * 32 + rr < ti.rows && cvalid)
+                                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16_raw*>(p.out) +
+                                                          (row0 + rr) * p.out_ld + fbase + c0 +
+                                                          8 * j) = w;
                         }
                     }
                 } else {
