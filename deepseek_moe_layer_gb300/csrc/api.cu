@@ -158,10 +158,12 @@ RouterPlan router_plan(int64_t T, int32_t d, int32_t E) {
         ttiles = (T + 127) / 128;
         ftiles = (E + 255) / 256;
     }
+    // K-split to spread the router weights over the SMs, but at least 8 k-blocks per split:
+    // every split adds a partial-logit matrix that the gate must read back
     const int nkb = d / 64;
     rp.ksplit = 1;
     for (int ks = 1; ks <= nkb; ++ks)
-        if (nkb % ks == 0 && ttiles * ftiles * ks <= nsm) rp.ksplit = ks;
+        if (nkb % ks == 0 && ttiles * ftiles * ks <= nsm && nkb / ks >= 8) rp.ksplit = ks;
     rp.tiles = ttiles * ftiles * rp.ksplit;
     return rp;
 }

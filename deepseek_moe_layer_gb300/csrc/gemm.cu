@@ -102,10 +102,14 @@ struct Cfg {
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kPrefixOff = kMiscOff + 16;
     static constexpr int kRowOffOff = kPrefixOff + 4 * (kMaxGroups + 1);
-    // bf16 gate/up and down with tokens on M: each epilogue warp stages 32 rows x 64 bf16
-    // (4 KB) so that its global stores cover whole 128-byte lines
+    // down with tokens on M (256 outputs per row and tile, a 2048-long main loop): each
+    // epilogue warp stages 32 rows x kStgCols bf16 (4 KB: whole 128-byte lines; 2 KB on the
+    // quantised paths: half lines) so that its global stores are row segments instead of one
+    // 16-byte piece per row (measured: prefill down 1.99 -> 1.74 ms; the gate/up GEMM, with
+    // half the outputs per tile and a 3.5x longer main loop, gained nothing)
     static constexpr int kEpiOff = (kRowOffOff + 4 * (kMaxGroups + 1) + 127) / 128 * 128;
-    static constexpr int kEpiBytes = (MODE != kRouter && !kSwap && !kQ) ? 4 * 4096 : 0;
+    static constexpr int kStgCols = kQ ? 32 : 64;  // the quantised rings leave room for 8 KB
+    static constexpr int kEpiBytes = (MODE == kDown && !kSwap) ? 4 * 32 * kStgCols * 2 : 0;
     static constexpr int kSmemBytes = kEpiOff + kEpiBytes + 1024;  // + align
     static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(kEpiOff % 16 == 0, "16-byte shared accesses of the staging buffer");
@@ -179,6 +183,38 @@ MOE_DEV uint4 dequant8_u8(uint32_t w0, uint32_t w1, float sc, float bi) {
     for (int i = 0; i < 4; ++i)
         r[i] = pack_bf16x2(fmaf(sc, q[2 * i], bi), fmaf(sc, q[2 * i + 1], bi));
     return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Staged epilogue stores.  A warp's 32 accumulator rows (one per lane) are written to a
+// shared buffer of 32 rows x COLS bf16 as 16-byte chunks, then read back with COLS/8 lanes per
+// row so that each warp store covers whole row segments (a 128-byte line for 64 columns, half
+// a line for 32).  The chunk index is XOR-swizzled with the row so that both the row-per-lane
+// writes and the segment-per-lanes reads are free of bank conflicts.
+template <int COLS>
+MOE_DEV int stage_chunk(int r, int j) {
+    return COLS == 64 ? (j ^ (r & 7)) : (j ^ ((r >> 1) & 3));
+}
+template <int COLS>
+MOE_DEV void stage_put(uint8_t* stg, int r, int j, uint4 v) {
+    *reinterpret_cast<uint4*>(stg + r * (COLS * 2) + (stage_chunk<COLS>(r, j) << 4)) = v;
+}
+// Row rr (< 32) of the staging buffer goes to out[row0 + rr][col0 + 8j .. +7] when the row
+// is one of the tile's `rows` valid ones (rr + rbase < rows) and the columns lie below F.
+template <int COLS>
+MOE_DEV void staged_store(const uint8_t* stg, int lane, __nv_bfloat16_raw* out, long long row0,
+                          long long ld, int col0, int rbase, int rows, int F) {
+    constexpr int kCh = COLS / 8;        // 16-byte chunks per staged row
+    constexpr int kRowsPer = 32 / kCh;   // rows per warp store
+    const int j = lane % kCh;
+    const bool cvalid = col0 + 8 * j + 8 <= F;  // F is a multiple of 8
+#pragma unroll
+    for (int it = 0; it < kCh; ++it) {
+        const int rr = it * kRowsPer + lane / kCh;
+        const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * (COLS * 2) +
+                                                         (stage_chunk<COLS>(rr, j) << 4));
+        if (rbase + rr < rows && cvalid)
+            *reinterpret_cast<uint4*>(out + (row0 + rr) * ld + col0 + 8 * j) = w;
+    }
 }
 
 MOE_DEV void fence_proxy_async_smem() {
@@ -702,14 +738,14 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                 const bool valid = r < ti.rows;
                 const long long orow = ti.out_row + r;
                 if (MODE == kGateUp && C::kEpiBytes > 0) {
-                    // h = silu(g) * u, 64 columns per staged chunk (as in the down epilogue)
-                    uint8_t* stg = smem + C::kEpiOff + q * 4096;
+                    // h = silu(g) * u, kStgCols columns per staged chunk (see staged_store)
+                    uint8_t* stg = smem + C::kEpiOff + q * (32 * C::kStgCols * 2);
                     const long long row0 = ti.out_row + q * 32;
                     const int fbase = ti.f * 128;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 128; c0 += 64) {
+                    for (int c0 = 0; c0 < 128; c0 += C::kStgCols) {
 #pragma unroll 1
-                        for (int hh = 0; hh < 2; ++hh) {
+                        for (int hh = 0; hh < C::kStgCols / 32; ++hh) {
                             uint32_t g[32], u[32];
                             __syncwarp();
                             tmem_ld32(tacc + c0 + 32 * hh, g);
@@ -725,24 +761,14 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                                         silu(__uint_as_float(g[c])) * __uint_as_float(u[c]),
                                         silu(__uint_as_float(g[c + 1])) * __uint_as_float(u[c + 1]));
                                 }
-                                const int j = 4 * hh + v;
-                                *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                                stage_put<C::kStgCols>(stg, lane, 4 * hh + v,
+                                                       make_uint4(w4[0], w4[1], w4[2], w4[3]));
                             }
                         }
                         __syncwarp();
-                        const int j = lane & 7;
-                        const bool cvalid = fbase + c0 + 8 * j + 8 <= p.F;  // F % 8 == 0
-#pragma unroll
-                        for (int it = 0; it < 8; ++it) {
-                            const int rr = it * 4 + (lane >> 3);
-                            const uint4 w =
-                                *reinterpret_cast<const uint4*>(stg + rr * 128 + ((j ^ (rr & 7)) << 4));
-                            if (q * 32 + rr < ti.rows && cvalid)
-                                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16_raw*>(p.out) +
-                                                          (row0 + rr) * p.out_ld + fbase + c0 +
-                                                          8 * j) = w;
-                        }
+                        staged_store<C::kStgCols>(stg, lane, static_cast<__nv_bfloat16_raw*>(p.out),
+                                                  row0, p.out_ld, fbase + c0, q * 32, ti.rows, p.F);
+                        __syncwarp();
                     }
                 } else if (MODE == kGateUp) {
                     __nv_bfloat16_raw* dst = static_cast<__nv_bfloat16_raw*>(p.out) +
@@ -771,41 +797,30 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                         }
                     }
                 } else if (MODE == kDown && C::kEpiBytes > 0) {
-                    // 64 columns at a time: this warp's 32 rows go to its staging buffer as
-                    // bf16 (16-byte chunk j of row r at chunk j ^ (r % 8): conflict-free), then
-                    // back out with 8 lanes per row, each warp store four whole 128-byte lines
-                    uint8_t* stg = smem + C::kEpiOff + q * 4096;
+                    uint8_t* stg = smem + C::kEpiOff + q * (32 * C::kStgCols * 2);
                     const int fbase = ti.f * 256;
                     const long long row0 = ti.out_row + q * 32;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 256 && fbase + c0 < p.F; c0 += 64) {
-                        uint32_t a[32], b[32];
-                        __syncwarp();
-                        tmem_ld32(tacc + c0, a);
-                        tmem_ld32(tacc + c0 + 32, b);
-                        tmem_ld_wait();
+                    for (int c0 = 0; c0 < 256 && fbase + c0 < p.F; c0 += C::kStgCols) {
+#pragma unroll 1
+                        for (int hh = 0; hh < C::kStgCols / 32; ++hh) {
+                            uint32_t a[32];
+                            __syncwarp();
+                            tmem_ld32(tacc + c0 + 32 * hh, a);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint32_t* v = j < 4 ? a + 8 * j : b + 8 * (j - 4);
-                            *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                                make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
-                                           pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
-                                           pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
-                                           pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
+                            for (int v = 0; v < 4; ++v)
+                                stage_put<C::kStgCols>(
+                                    stg, lane, 4 * hh + v,
+                                    make_uint4(pack_bf16x2(__uint_as_float(a[8 * v + 0]), __uint_as_float(a[8 * v + 1])),
+                                               pack_bf16x2(__uint_as_float(a[8 * v + 2]), __uint_as_float(a[8 * v + 3])),
+                                               pack_bf16x2(__uint_as_float(a[8 * v + 4]), __uint_as_float(a[8 * v + 5])),
+                                               pack_bf16x2(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7]))));
                         }
                         __syncwarp();
-                        const int j = lane & 7;
-                        const bool cvalid = fbase + c0 + 8 * j + 8 <= p.F;  // F % 8 == 0
-#pragma unroll
-                        for (int it = 0; it < 8; ++it) {
-                            const int rr = it * 4 + (lane >> 3);
-                            const uint4 w =
-                                *reinterpret_cast<const uint4*>(stg + rr * 128 + ((j ^ (rr & 7)) << 4));
-                            if (q * 32 + rr < ti.rows && cvalid)
-                                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16_raw*>(p.out) +
-                                                          (row0 + rr) * p.out_ld + fbase + c0 +
-                                                          8 * j) = w;
-                        }
+                        staged_store<C::kStgCols>(stg, lane, static_cast<__nv_bfloat16_raw*>(p.out),
+                                                  row0, p.out_ld, fbase + c0, q * 32, ti.rows, p.F);
+                        __syncwarp();
                     }
                 } else {
                     const int fbase = ti.f * 256;
