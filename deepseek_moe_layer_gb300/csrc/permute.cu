@@ -123,17 +123,18 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     const long long t = perm[j] / K;
     const uint4* src = x + t * vec_per_row;
     uint4* dst = x_perm + j * vec_per_row;
-    // four 16-byte loads in flight per lane before the stores
+    // four 16-byte loads in flight per lane before the stores; the gathered rows are
+    // streamed out (evict-first) so that x, read K times, stays in L2
     int v = lane;
     for (; v + 96 < vec_per_row; v += 128) {
         const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
                     e = __ldg(src + v + 96);
-        dst[v] = a;
-        dst[v + 32] = b;
-        dst[v + 64] = c;
-        dst[v + 96] = e;
+        __stcs(dst + v, a);
+        __stcs(dst + v + 32, b);
+        __stcs(dst + v + 64, c);
+        __stcs(dst + v + 96, e);
     }
-    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    for (; v < vec_per_row; v += 32) __stcs(dst + v, __ldg(src + v));
 }
 
 }  // namespace
