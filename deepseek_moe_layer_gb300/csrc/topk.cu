@@ -223,9 +223,31 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
     __syncthreads();
 
     // four keys of this CTA's segment starting at i (a multiple of 4)
+    // uncached segments: four keys by one 16-byte (fp32) or 8-byte (bf16) load when the row
+    // allows it (j0 and i are multiples of 4 here), else one key at a time
+    const bool gvec = ((reinterpret_cast<uintptr_t>(srow) +
+                        (uintptr_t)j0 * (BF16 ? 2u : 4u)) & (BF16 ? 7u : 15u)) == 0;
     auto get4 = [&](int i) -> uint4 {
         if constexpr (CACHED) return keys4(keys, i, cnt);
         uint4 q;
+        if (gvec && i + 3 < cnt) {
+            if (BF16) {
+                const uint2 w = __ldg(reinterpret_cast<const uint2*>(
+                    static_cast<const uint16_t*>(srow) + j0 + i));
+                q.x = score_key(__uint_as_float(w.x << 16));
+                q.y = score_key(__uint_as_float(w.x & 0xFFFF0000u));
+                q.z = score_key(__uint_as_float(w.y << 16));
+                q.w = score_key(__uint_as_float(w.y & 0xFFFF0000u));
+            } else {
+                const float4 f = __ldg(reinterpret_cast<const float4*>(
+                    static_cast<const float*>(srow) + j0 + i));
+                q.x = score_key(f.x);
+                q.y = score_key(f.y);
+                q.z = score_key(f.z);
+                q.w = score_key(f.w);
+            }
+            return q;
+        }
         q.x = i < cnt ? load_key<BF16>(srow, j0 + i) : 0u;
         q.y = i + 1 < cnt ? load_key<BF16>(srow, j0 + i + 1) : 0u;
         q.z = i + 2 < cnt ? load_key<BF16>(srow, j0 + i + 2) : 0u;
@@ -248,12 +270,12 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
     int kk0 = k;               // rank of the threshold among the radix select's keys
     int ccnt = 0;              // candidates of this CTA
     uint32_t above_win = 0;    // this CTA's keys above the window
-    if (kWin && cached && (long long)k * 8 <= nr) {  // sparse selections (decode-like rows)
+    if (kWin && (long long)k * 8 <= nr) {  // sparse selections (decode-like rows)
         const int stride = (nr + kSample - 1) / kSample;
         const int ns = (nr + stride - 1) / stride;  // <= kSample
         uint32_t* samp0 = nc > 1 ? cl.map_shared_rank(samp, 0) : samp;
         for (int j = (j0 + stride - 1) / stride * stride + tid * stride; j < v1; j += THREADS * stride)
-            samp0[j / stride] = keys[j - j0];
+            samp0[j / stride] = CACHED ? keys[j - j0] : load_key<BF16>(srow, j);
         csync();
         if (rank == 0) {
             int n2 = 1;
@@ -285,7 +307,7 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
         uint32_t a = 0, wn = 0;
         for (int base = 0; base < cnt; base += 4 * THREADS) {
             const int i = base + 4 * tid;
-            const uint4 q = keys4(keys, i, cnt);
+            const uint4 q = get4(i);
             const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -317,7 +339,7 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
             __syncthreads();
             for (int base = 0; base < cnt; base += 4 * THREADS) {
                 const int i = base + 4 * tid;
-                const uint4 q = keys4(keys, i, cnt);
+                const uint4 q = get4(i);
                 const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -336,7 +358,7 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
     // the radix select's keys: the candidates, or every key of the segment
     auto getr4 = [&](int i) -> uint4 {
         if constexpr (CACHED) return keys4(windowed ? cand : keys, i, windowed ? ccnt : cnt);
-        return get4(i);
+        return windowed ? keys4(cand, i, ccnt) : get4(i);
     };
     const int rcnt = windowed ? ccnt : cnt;
 
@@ -530,7 +552,9 @@ constexpr int kShortRow = 8192;  // segments up to this many keys take the short
 
 void indexer_topk_plan(TopkArgs& a) {
     // segments of at most kSegMax keys (64 KB of shared memory) per CTA, up to 8 CTAs per
-    // row; longer rows keep 8 CTAs and re-read their keys from global memory in every pass
+    // row; longer rows keep 8 CTAs and re-read their keys from global memory (L2 after the
+    // first pass) in every pass.  (Re-reading was also measured for many rows of cacheable
+    // length: slower, as registers hold the kernel to 2 CTAs per SM either way.)
     constexpr int kSegMax = 16384;
     long long nc = (a.n + kSegMax - 1) / kSegMax;
     nc = nc < 1 ? 1 : (nc > 8 ? 8 : nc);

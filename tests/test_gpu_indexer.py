@@ -39,6 +39,19 @@ def test_indexer_topk_shapes(rows, n, k):
     _check(torch.randn(rows, n, generator=g, device=DEV), k)
 
 
+def test_indexer_topk_rows_too_long_to_cache():
+    # rows longer than 8 x 16384 keys: the keys stay in global memory (L2), sparse rows take
+    # the sampled window, dense ones the full radix select
+    g = torch.Generator(device=DEV).manual_seed(11)
+    _check(torch.randn(3, 200000, generator=g, device=DEV), 2048)
+    _check((torch.randn(3, 150000, generator=g, device=DEV) * 2).to(torch.bfloat16), 1024)
+    big = torch.randn(2, 160003, generator=g, device=DEV)
+    _check(big[:, 3:], 700)  # misaligned rows: scalar loads
+    ties = torch.randint(-3, 4, (3, 140000), generator=g, device=DEV).float()
+    _check(ties, 2048)
+    _check(torch.randn(2, 140000, generator=g, device=DEV), 40000)  # dense: no window
+
+
 def test_indexer_topk_workload_scores_small():
     w = inputs.INDEXER_WORKLOADS["dsa_small_R37_N5000"]
     _check(inputs.gen_indexer_scores(w, DEV, seed=1), w.k)
