@@ -29,7 +29,7 @@ namespace {
 namespace cg = cooperative_groups;
 
 constexpr unsigned kAll = 0xFFFFFFFFu;
-constexpr int kSample = 512;    // keys sampled per row for the threshold window
+constexpr int kSample = 2048;   // keys sampled per row for the threshold window
 constexpr int kCandCap = 4096;  // window keys a CTA can hold
 
 // Order-preserving key of an fp32 score: NaN -> 0 (lowest), -0 -> +0.
@@ -115,7 +115,9 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
     __shared__ int s_counts[2];             // this CTA's (greater, equal) counts
     __shared__ int s_wcnt[2];               // keys above / inside the window
     __shared__ uint32_t s_win[2];           // window (low, high) keys, set by the leader
-    __shared__ int s_ccnt;                  // candidates written
+    __shared__ int s_sel[4];                // leader: the sample's first digits and ranks
+    __shared__ int s_cg[8], s_ce[8];        // leader: every CTA's keys above / equal to tau
+    __shared__ uint32_t s_res[3];           // from the leader: tau, output base, ties to take
 
     const int n = a.n, k = a.k;
     int nr = a.lengths ? a.lengths[row] : n;
@@ -264,12 +266,19 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
     // keys delta ranks above and below the k-th largest's expected rank, and the cluster
     // counts exactly how many keys lie above and inside that window (register counters, no
     // atomics).  When the k-th largest provably lies inside, only the window's keys (the
-    // candidates) enter the radix select; otherwise every key does.
-    bool windowed = false;
+    // candidates) enter the radix select.  If all of the row's candidates fit one CTA's
+    // buffer, every CTA writes its candidates into the leader's, and the leader alone selects
+    // the threshold and hands every CTA its output base and share of the ties (no cluster
+    // barrier in its radix passes); otherwise each CTA keeps its own candidates and the
+    // cluster merges its histograms pass by pass.  Without a window the cluster's radix
+    // select runs over every key.
+    bool windowed = false, leader = false;
+    int c_above = 0, c_win = 0, c_off = 0;  // leader mode, warp c: CTA c's window counts
     uint32_t wlo = 0u, whi = 0xFFFFFFFFu;  // the window (inclusive), when windowed
     int kk0 = k;               // rank of the threshold among the radix select's keys
     int ccnt = 0;              // candidates of this CTA
     uint32_t above_win = 0;    // this CTA's keys above the window
+    static_assert(!kWin || (NB == 2048 && THREADS == 512), "the sample select: 4 bins a thread");
     if (kWin && (long long)k * 8 <= nr) {  // sparse selections (decode-like rows)
         const int stride = (nr + kSample - 1) / kSample;
         const int ns = (nr + stride - 1) / stride;  // <= kSample
@@ -278,26 +287,64 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
             samp0[j / stride] = CACHED ? keys[j - j0] : load_key<BF16>(srow, j);
         csync();
         if (rank == 0) {
-            int n2 = 1;
-            while (n2 < ns) n2 <<= 1;
-            for (int i = ns + tid; i < n2; i += THREADS) samp[i] = 0u;
+            // the sample's keys of (0-based, descending) ranks r - delta and r + delta, to
+            // their top 22 bits: two radix passes of 11 bits, both ranks in the same passes
+            // (counts of the two targets packed into the halves of one scanned word)
+            const int r = (int)((long long)k * ns / nr);
+            const int delta = 3 * (int)sqrtf((float)r) + 8;  // ~3 sigma of the sample rank
+            const int kka = r - delta + 1, kkb = r + delta + 1;  // 1-based ranks; a: high end
+            for (int b = tid; b < 2048; b += THREADS) hist[b] = 0;
             __syncthreads();
-            // bitonic sort, descending
-            for (int size = 2; size <= n2; size <<= 1)
-                for (int st = size >> 1; st > 0; st >>= 1) {
-                    for (int i = tid; i < (n2 >> 1); i += THREADS) {
-                        const int lo = 2 * i - (i & (st - 1)), hi = lo + st;  // st: power of 2
-                        const bool desc = (lo & size) == 0;
-                        const uint32_t x = samp[lo], y = samp[hi];
-                        if ((x < y) == desc) { samp[lo] = y; samp[hi] = x; }
-                    }
-                    __syncthreads();
+            for (int i = tid; i < ns; i += THREADS) atomicAdd(&hist[samp[i] >> 21], 1);
+            __syncthreads();
+            {
+                const int hi = 2047 - 4 * tid;  // this thread's bins, top-down
+                uint32_t mine = 0, total;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) mine += (uint32_t)hist[hi - q];
+                uint32_t acc = block_excl_scan<THREADS>(mine, s_warp, &total);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t c = (uint32_t)hist[hi - q];
+                    if ((int)acc < kka && (int)(acc + c) >= kka) { s_sel[0] = hi - q; s_sel[1] = kka - (int)acc; }
+                    if ((int)acc < kkb && (int)(acc + c) >= kkb) { s_sel[2] = hi - q; s_sel[3] = kkb - (int)acc; }
+                    acc += c;
                 }
-            if (tid == 0) {
-                const int r = (int)((long long)k * ns / nr);
-                const int delta = 3 * (int)sqrtf((float)r) + 8;  // ~3 sigma of the sample rank
-                s_win[0] = r + delta < ns ? samp[r + delta] : 0u;          // low end
-                s_win[1] = r - delta >= 0 ? samp[r - delta] : 0xFFFFFFFFu;  // high end
+            }
+            __syncthreads();
+            const int da = kka >= 1 ? s_sel[0] : -1, db = kkb <= ns ? s_sel[2] : -1;
+            for (int b = tid; b < 2048; b += THREADS) { hist[b] = 0; merged[b] = 0; }
+            __syncthreads();
+            for (int i = tid; i < ns; i += THREADS) {
+                const uint32_t key = samp[i];
+                const int top = (int)(key >> 21), mid = (int)((key >> 10) & 0x7FFu);
+                if (top == da) atomicAdd(&hist[mid], 1);
+                if (top == db) atomicAdd(&merged[mid], 1);
+            }
+            __syncthreads();
+            {
+                const int hi = 2047 - 4 * tid;
+                uint32_t mine = 0, total;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    mine += (uint32_t)hist[hi - q] | ((uint32_t)merged[hi - q] << 16);
+                const uint32_t before = block_excl_scan<THREADS>(mine, s_warp, &total);
+                int acca = (int)(before & 0xFFFFu), accb = (int)(before >> 16);
+                const int ra = s_sel[1], rb = s_sel[3];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int ca = hist[hi - q], cb = merged[hi - q];
+                    if (da >= 0 && acca < ra && acca + ca >= ra)
+                        s_win[1] = ((uint32_t)da << 21) | ((uint32_t)(hi - q) << 10) | 0x3FFu;
+                    if (db >= 0 && accb < rb && accb + cb >= rb)
+                        s_win[0] = ((uint32_t)db << 21) | ((uint32_t)(hi - q) << 10);
+                    acca += ca;
+                    accb += cb;
+                }
+                if (tid == 0) {
+                    if (da < 0) s_win[1] = 0xFFFFFFFFu;  // no high end
+                    if (db < 0) s_win[0] = 0u;           // no low end
+                }
             }
         }
         csync();
@@ -318,152 +365,214 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
         }
         uint32_t ta, tw;
         block_excl_scan<THREADS>(a, s_warp, &ta);
-        block_excl_scan<THREADS>(wn, s_warp, &tw);
+        const uint32_t wpre = block_excl_scan<THREADS>(wn, s_warp, &tw);  // this thread's slot
         if (tid == 0) { s_wcnt[0] = (int)ta; s_wcnt[1] = (int)tw; }
         csync();
-        long long G = 0, Wt = 0;
-        bool fits = true;
-        for (unsigned c = 0; c < nc; ++c) {
-            const int* rc = c == rank ? s_wcnt : cl.map_shared_rank(s_wcnt, c);
-            G += rc[0];
-            Wt += rc[1];
-            fits = fits && rc[1] <= kCandCap;
+        int ca[8], cw[8];  // every CTA's counts, all remote loads in flight together
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            ca[c] = cw[c] = 0;
+            if (c < (int)nc) {
+                const int* rc = c == (int)rank ? s_wcnt : cl.map_shared_rank(s_wcnt, c);
+                ca[c] = rc[0];
+                cw[c] = rc[1];
+            }
         }
-        csync();  // the counts were read: s_wcnt may be reused
-        windowed = fits && G < k && G + Wt >= k;
+        long long G = 0, Wt = 0, off = 0;
+        int wmax = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            if (c == warp) { c_above = ca[c]; c_win = cw[c]; c_off = (int)Wt; }
+            if (c < (int)rank) off += cw[c];
+            G += ca[c];
+            Wt += cw[c];
+            wmax = cw[c] > wmax ? cw[c] : wmax;
+        }
+        // (s_wcnt, s_win and the sample are never written again: no barrier here)
+        windowed = wmax <= kCandCap && G < k && G + Wt >= k;
+        leader = windowed && nc > 1 && Wt <= kCandCap;
         if (windowed) {
             kk0 = k - (int)G;
             above_win = ta;
-            // candidates into shared memory, in any order (warp-aggregated slots)
-            if (tid == 0) s_ccnt = 0;
-            __syncthreads();
+            ccnt = leader ? (int)Wt : (int)tw;
+            // this CTA's candidates (thread by thread, each at its prefix of the window counts)
+            // into the leader's buffer from `off` on, or into its own
+            uint32_t* dst = (leader ? cl.map_shared_rank(cand, 0) + off : cand) + wpre;
+            int j = 0;
             for (int base = 0; base < cnt; base += 4 * THREADS) {
                 const int i = base + 4 * tid;
                 const uint4 q = get4(i);
                 const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const bool in = i + e < cnt && kq[e] >= wlo && kq[e] <= whi;
-                    const unsigned m = __ballot_sync(kAll, in);
-                    int slot = 0;
-                    if (lane == 0 && m) slot = atomicAdd(&s_ccnt, __popc(m));
-                    slot = __shfl_sync(kAll, slot, 0);
-                    if (in) cand[slot + __popc(m & ((1u << lane) - 1u))] = kq[e];
-                }
+                for (int e = 0; e < 4; ++e)
+                    if (i + e < cnt && kq[e] >= wlo && kq[e] <= whi) dst[j++] = kq[e];
             }
-            __syncthreads();
-            ccnt = s_ccnt;
+            if (leader) csync();  // every candidate is in the leader's buffer
+            else __syncthreads();
         }
     }
-    // the radix select's keys: the candidates, or every key of the segment
-    auto getr4 = [&](int i) -> uint4 {
-        if constexpr (CACHED) return keys4(windowed ? cand : keys, i, windowed ? ccnt : cnt);
-        return windowed ? keys4(cand, i, ccnt) : get4(i);
-    };
-    const int rcnt = windowed ? ccnt : cnt;
-
-    // ---- radix select of the k-th largest key over the cluster ----
-    // Over the candidates the digits are those of key - wlo, 8 bits at a time, over only the
-    // window's significant bits: small histograms keep the cluster merges cheap.
-    const int dbits = windowed ? 8 : DBITS;
-    const uint32_t kbase = windowed ? wlo : 0u;
-    const int nbits = windowed ? (whi == wlo ? 1 : 32 - __clz((int)(whi - wlo))) : 32;
-    const int npass = (nbits + dbits - 1) / dbits;
-    uint32_t prefix = 0, pmask = 0;
-    int kk = kk0;         // elements still to take among those matching the prefix
-    uint32_t my_gt = 0;   // this thread's share of the CTA's count of keys above the result
+    // ---- radix select of the k-th largest key ----
+    // run(merge): over the candidates (leader only, merge = false) or over every key of the
+    // segment with the cluster's histograms summed through distributed shared memory.  Over
+    // the candidates the digits are those of key - wlo, 8 bits at a time, over only the
+    // window's significant bits.
+    uint32_t tau = 0;
+    int kk = kk0;            // elements equal to tau still to take
+    uint32_t my_gt = 0;      // this thread's share of the CTA's count of keys above tau
     int last_digit = 0;
+    auto radix = [&](bool merge) {
+        // (8-bit digits where the cluster merges its histograms over distributed shared memory)
+        const int dbits = windowed && merge ? 8 : DBITS;
+        const uint32_t kbase = windowed ? wlo : 0u;
+        const int nbits = windowed ? (whi == wlo ? 1 : 32 - __clz((int)(whi - wlo))) : 32;
+        const int npass = (nbits + dbits - 1) / dbits;
+        const int rcnt = windowed ? ccnt : cnt;
+        auto getr4 = [&](int i) -> uint4 { return windowed ? keys4(cand, i, ccnt) : get4(i); };
+        uint32_t prefix = 0, pmask = 0;
 #pragma unroll 1
-    for (int pass = 0; pass < npass; ++pass) {
-        const int top = nbits - dbits * pass;
-        const int shift = top > dbits ? top - dbits : 0;
-        const int nb = 1 << (top - shift);
-        for (int b = tid; b < nb; b += THREADS) hist[b] = 0;
-        __syncthreads();
-        for (int base = 0; base < rcnt; base += 4 * THREADS) {
-            const int i = base + 4 * tid;
-            const uint4 q = getr4(i);
-            const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
-            bool want[4];
-            bool any = false;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                want[e] = i + e < rcnt && ((kq[e] - kbase) & pmask) == prefix;
-                any |= want[e];
-            }
-            if (pass == 0 || __any_sync(kAll, any)) {
+        for (int pass = 0; pass < npass; ++pass) {
+            const int top = nbits - dbits * pass;
+            const int shift = top > dbits ? top - dbits : 0;
+            const int nb = 1 << (top - shift);
+            for (int b = tid; b < nb; b += THREADS) hist[b] = 0;
+            __syncthreads();
+            for (int base = 0; base < rcnt; base += 4 * THREADS) {
+                const int i = base + 4 * tid;
+                const uint4 q = getr4(i);
+                const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+                bool want[4];
+                bool any = false;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const uint32_t bin = ((kq[e] - kbase) >> shift) & (uint32_t)(nb - 1);
-                    if (want[e]) atomicAdd(&hist[bin], 1);
+                    want[e] = i + e < rcnt && ((kq[e] - kbase) & pmask) == prefix;
+                    any |= want[e];
+                }
+                if (pass == 0 || __any_sync(kAll, any)) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t bin = ((kq[e] - kbase) >> shift) & (uint32_t)(nb - 1);
+                        if (want[e]) atomicAdd(&hist[bin], 1);
+                    }
+                }
+            }
+            const int* tot = hist;
+            if (merge && nc > 1) {
+                cl.sync();  // every CTA's histogram is complete
+                for (int b = tid; b < nb; b += THREADS) {
+                    int sum = 0;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        if (c < (int)nc)
+                            sum += c == (int)rank ? hist[b] : cl.map_shared_rank(hist, c)[b];
+                    merged[b] = sum;
+                }
+                cl.sync();  // no CTA reads another's histogram any more
+                tot = merged;
+            } else {
+                __syncthreads();
+            }
+            // digit: the bin where the count of larger digits < kk <= that count plus the
+            // bin; thread t owns bins hi, hi-1, .., hi-per+1 (top-down), hi = nb - 1 - t*per
+            const int per = nb >= THREADS ? nb / THREADS : 1;
+            const int hi = nb - 1 - tid * per;
+            uint32_t mine = 0;
+            for (int q = 0; q < per && hi - q >= 0; ++q) mine += (uint32_t)tot[hi - q];
+            uint32_t total;
+            const uint32_t above = block_excl_scan<THREADS>(mine, s_warp, &total);
+            uint32_t acc = above;
+            for (int q = 0; q < per && hi - q >= 0; ++q) {
+                const uint32_t c = (uint32_t)tot[hi - q];
+                if (acc < (uint32_t)kk && acc + c >= (uint32_t)kk) {
+                    s_pick[0] = hi - q;
+                    s_pick[1] = kk - (int)acc;
+                }
+                acc += c;
+            }
+            __syncthreads();
+            const int d = s_pick[0];
+            // this CTA's keys in the bins above the digit are above the final threshold
+            for (int q = 0; q < per && hi - q > d; ++q) my_gt += (uint32_t)hist[hi - q];
+            prefix |= (uint32_t)d << shift;
+            pmask |= (uint32_t)(nb - 1) << shift;
+            kk = s_pick[1];
+            last_digit = d;
+            __syncthreads();
+        }
+        tau = prefix + kbase;
+    };
+
+    int out_base = 0, take = 0;  // this CTA's first output slot; threshold ties it takes
+    if (leader) {
+        if (rank == 0) {
+            radix(false);
+            // CTA c's keys above / equal to tau: its keys above the window plus those of its
+            // candidates (warp c counts CTA c's range of the buffer)
+            if (warp < (int)nc) {
+                uint32_t g = 0, e = 0;
+                for (int i = lane; i < c_win; i += 32) {
+                    const uint32_t x = cand[c_off + i];
+                    g += x > tau;
+                    e += x == tau;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    g += __shfl_xor_sync(kAll, g, o);
+                    e += __shfl_xor_sync(kAll, e, o);
+                }
+                if (lane == 0) { s_cg[warp] = c_above + (int)g; s_ce[warp] = (int)e; }
+            }
+            __syncthreads();
+            if (tid == 0) {  // ties lowest position first: CTAs in rank order
+                int rem = kk, base = 0;
+                for (int c = 0; c < (int)nc; ++c) {
+                    const int t = s_ce[c] < rem ? s_ce[c] : rem;
+                    uint32_t* r = c == 0 ? s_res : cl.map_shared_rank(s_res, c);
+                    r[0] = tau;
+                    r[1] = (uint32_t)base;
+                    r[2] = (uint32_t)t;
+                    base += s_cg[c] + t;
+                    rem -= t;
                 }
             }
         }
-        const int* tot = hist;
+        cl.sync();  // every CTA's results are in place; no remote access from here on
+        tau = s_res[0];
+        out_base = (int)s_res[1];
+        take = (int)s_res[2];
+    } else {
+        radix(true);
+        uint32_t cta_gt;
+        block_excl_scan<THREADS>(my_gt, s_warp, &cta_gt);
+        if (tid == 0) {
+            s_counts[0] = (int)(cta_gt + above_win);
+            s_counts[1] = hist[last_digit];  // keys equal to tau in this CTA
+        }
+        // each CTA's share of the threshold ties (lowest position first) and its output base
+        int rem = kk;
         if (nc > 1) {
-            cl.sync();  // every CTA's histogram is complete
-            for (int b = tid; b < nb; b += THREADS) {
-                int sum = 0;
-                for (unsigned c = 0; c < nc; ++c)
-                    sum += c == rank ? hist[b] : cl.map_shared_rank(hist, c)[b];
-                merged[b] = sum;
+            cl.sync();
+            int cg_[8], ce_[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                cg_[c] = ce_[c] = 0;
+                if (c < (int)nc) {
+                    const int* rc = c == (int)rank ? s_counts : cl.map_shared_rank(s_counts, c);
+                    cg_[c] = rc[0];
+                    ce_[c] = rc[1];
+                }
             }
-            cl.sync();  // no CTA reads another's histogram any more
-            tot = merged;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int t = ce_[c] < rem ? ce_[c] : rem;
+                if (c < (int)rank) out_base += cg_[c] + t;
+                if (c == (int)rank) take = t;
+                rem -= t;
+            }
+            cl.sync();  // remote counts read: no CTA touches another's shared memory from here on
         } else {
             __syncthreads();
+            take = s_counts[1] < rem ? s_counts[1] : rem;
         }
-        // digit: the bin where the count of larger digits < kk <= that count plus the bin;
-        // thread t owns bins hi, hi-1, .., hi-per+1 (top-down), hi = nb - 1 - t*per
-        const int per = nb >= THREADS ? nb / THREADS : 1;
-        const int hi = nb - 1 - tid * per;
-        uint32_t mine = 0;
-        for (int q = 0; q < per && hi - q >= 0; ++q) mine += (uint32_t)tot[hi - q];
-        uint32_t total;
-        const uint32_t above = block_excl_scan<THREADS>(mine, s_warp, &total);
-        uint32_t acc = above;
-        for (int q = 0; q < per && hi - q >= 0; ++q) {
-            const uint32_t c = (uint32_t)tot[hi - q];
-            if (acc < (uint32_t)kk && acc + c >= (uint32_t)kk) {
-                s_pick[0] = hi - q;
-                s_pick[1] = kk - (int)acc;
-            }
-            acc += c;
-        }
-        __syncthreads();
-        const int d = s_pick[0];
-        // this CTA's keys in the bins above the digit are above the final threshold
-        for (int q = 0; q < per && hi - q > d; ++q) my_gt += (uint32_t)hist[hi - q];
-        prefix |= (uint32_t)d << shift;
-        pmask |= (uint32_t)(nb - 1) << shift;
-        kk = s_pick[1];
-        last_digit = d;
-        __syncthreads();
-    }
-    const uint32_t tau = prefix + kbase;  // key of the k-th largest; kk of the keys equal to it are taken
-
-    // ---- this CTA's counts, its share of the threshold ties and its output base ----
-    uint32_t cta_gt;
-    block_excl_scan<THREADS>(my_gt, s_warp, &cta_gt);
-    if (tid == 0) {
-        s_counts[0] = (int)(cta_gt + above_win);
-        s_counts[1] = hist[last_digit];  // keys equal to tau in this CTA
-    }
-    int rem = kk, out_base = 0, take = 0;
-    if (nc > 1) {
-        cl.sync();
-        for (unsigned c = 0; c < nc; ++c) {
-            const int* rc = c == rank ? s_counts : cl.map_shared_rank(s_counts, c);
-            const int g = rc[0], e = rc[1];
-            const int t = e < rem ? e : rem;
-            if (c < rank) out_base += g + t;
-            if (c == rank) take = t;
-            rem -= t;
-        }
-        cl.sync();  // remote counts read: no CTA touches another's shared memory from here on
-    } else {
-        __syncthreads();
-        take = s_counts[1] < rem ? s_counts[1] : rem;
     }
 
     // ---- compaction in position order: each warp a contiguous range, 4 keys per lane ----

@@ -50,6 +50,8 @@ def test_indexer_topk_rows_too_long_to_cache():
     ties = torch.randint(-3, 4, (3, 140000), generator=g, device=DEV).float()
     _check(ties, 2048)
     _check(torch.randn(2, 140000, generator=g, device=DEV), 40000)  # dense: no window
+    # a window wider than one CTA's candidate buffer: each CTA keeps its own candidates
+    _check(torch.randn(2, 1 << 20, generator=g, device=DEV), 2048)
 
 
 def test_indexer_topk_workload_scores_small():
