@@ -40,6 +40,7 @@ def test_routing_workload_16384x256(p):
     (16, 4, 2, 4), (16, 1, 1, 16), (8, 4, 1, 1), (32, 8, 3, 6), (64, 8, 4, 8),
     (96, 4, 2, 8), (96, 12, 5, 7), (160, 8, 4, 8), (48, 16, 5, 3), (256, 8, 4, 8),
     (256, 1, 1, 32), (512, 32, 8, 16), (1024, 16, 4, 32), (1024, 1, 1, 1), (20, 10, 3, 5),
+    (128, 4, 2, 8), (128, 2, 1, 5), (256, 4, 3, 7), (64, 1, 1, 8), (256, 8, 8, 8), (64, 2, 1, 1),
 ])
 @pytest.mark.parametrize("norm", [True, False])
 def test_route_shapes(E, G, tg, K, norm):
@@ -49,7 +50,8 @@ def test_route_shapes(E, G, tg, K, norm):
     _run(logits, bias, K, G, tg, norm, 2.5)
 
 
-@pytest.mark.parametrize("E,G,tg,K", [(16, 4, 2, 4), (12, 3, 1, 5), (64, 8, 2, 12), (96, 12, 5, 7)])
+@pytest.mark.parametrize("E,G,tg,K", [(16, 4, 2, 4), (12, 3, 1, 5), (64, 8, 2, 12), (96, 12, 5, 7),
+                                     (64, 8, 2, 8), (128, 4, 2, 8), (256, 8, 4, 8), (256, 2, 1, 6)])
 def test_route_exact_ties(E, G, tg, K):
     # integer logits and quarter-integer biases: many exact ties between experts and groups
     g = torch.Generator(device=DEV).manual_seed(E + 7 * K)
