@@ -62,13 +62,22 @@ template <int MODE, int TOKT, int QB>
 struct Cfg {
     static constexpr bool kQ = QB != 0;                              // affine-quantised weights
     static constexpr bool kSwap = TOKT != 0;
-    static constexpr int kTok = kSwap ? TOKT : 128;                  // tokens per tile
+    // quantised experts with tokens on M: a tile is two 128-row token sub-tiles that share
+    // every dequantised weight stage (each B tile feeds two UMMAs, one accumulator per
+    // sub-tile), which halves the dequantisation work per flop.  The two accumulators fill
+    // TMEM, so they are single-buffered.  (Measured: 4-bit prefill T=4096 5.18 -> 3.90 ms;
+    // the bf16 experts, whose weight tiles arrive by TMA, lose more to the single-buffered
+    // accumulators than they gain: 5.72 -> 6.17 ms at T=8192, so they keep 128-row tiles.)
+    static constexpr bool kM2 = kQ && !kSwap && MODE != kRouter;
+    static constexpr int kSub = kM2 ? 2 : 1;                         // token sub-tiles
+    static constexpr int kTok = kSwap ? TOKT : 128 * kSub;           // tokens per tile
     static constexpr int kNW = (kSwap && MODE == kGateUp) ? 2 : 1;   // A weight tiles (swap)
     static constexpr int kWRows = kSwap ? 128 * kNW : 256;           // weight rows per stage
     static constexpr int kFeat = kSwap ? 128 : (MODE == kGateUp ? 128 : 256);
     static constexpr int kXBytes = kTok * 128;
     static constexpr int kWBytes = kWRows * 128;
-    static constexpr int kAccCols = kSwap ? kTok * kNW : 256;
+    static constexpr int kAccCols = kSwap ? kTok * kNW : 256 * kSub;
+    static constexpr int kAccBufs = kM2 ? 1 : 2;                     // accumulator buffers
     // 4-bit with tokens on N ("TMEM-A" path): the dequant warps write the bf16 weights
     // straight into TMEM (tcgen05.st) and the UMMA reads its A operand from there, so the
     // dequantised tile never crosses shared memory (which would otherwise carry 8x the HBM
@@ -91,7 +100,7 @@ struct Cfg {
     static constexpr int kRawStages =
         !kQ ? 0 : kTA ? cmin(8, (216 * 1024 - kStages * kStageBytes) / kRBytes) : 2;
     static constexpr int kThreadsCta = kQ ? kThreads + 32 + 32 * kDequantWarps : kThreads;
-    static constexpr int kTmemCols = kTA ? 512 : pow2ceil(cmax(32, 2 * kAccCols));
+    static constexpr int kTmemCols = kTA ? 512 : pow2ceil(cmax(32, kAccBufs * kAccCols));
     static constexpr int kN = kSwap ? kTok : 256;
     static constexpr uint32_t kIdesc = idesc_bf16(128, kN);
     static constexpr int kMaxGroups = 1025;
@@ -471,8 +480,8 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
                 const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
-                const int ab = lt & 1;
-                const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+                const int ab = C::kAccBufs == 2 ? (lt & 1) : 0;
+                const uint32_t aph = (uint32_t)(C::kAccBufs == 2 ? (lt >> 1) : lt) & 1u;
                 if (!mbar_wait(&tempty[ab], aph ^ 1u, abort)) { record_timeout(abort); break; }
                 tc_fence_after();
                 const uint32_t acc = tmem_base + (uint32_t)(ab * C::kAccCols);
@@ -503,8 +512,12 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                                           sdesc_k128(ws + w * 128 * 128 + kk * 32), bd,
                                           C::kIdesc, accum);
                         } else {
-                            umma_bf16(acc, sdesc_k128(xs + kk * 32), sdesc_k128(ws + kk * 32),
-                                      C::kIdesc, accum);
+                            const uint64_t bd = sdesc_k128(ws + kk * 32);
+                            umma_bf16(acc, sdesc_k128(xs + kk * 32), bd, C::kIdesc, accum);
+                            // the second sub-tile's tokens, when the tile has any
+                            if (C::kM2 && ti.rows > 128)
+                                umma_bf16(acc + 256u, sdesc_k128(xs + 128 * 128 + kk * 32), bd,
+                                          C::kIdesc, accum);
                         }
                     }
                     umma_commit(&empty[s]);
@@ -726,21 +739,24 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
         int lt = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
             const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
-            const int ab = lt & 1;
-            const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+            const int ab = C::kAccBufs == 2 ? (lt & 1) : 0;
+            const uint32_t aph = (uint32_t)(C::kAccBufs == 2 ? (lt >> 1) : lt) & 1u;
             if (!mbar_wait(&tfull[ab], aph, abort)) { record_timeout(abort); break; }
             tc_fence_after();
-            const uint32_t tacc =
+            const uint32_t tacc0 =
                 tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kAccCols);
-            if (!C::kSwap) {
-                // accumulator row = token row (q*32 + lane), columns = features
-                const int r = q * 32 + lane;
+            if (!C::kSwap)
+#pragma unroll 1
+            for (int sub = 0; sub < C::kSub && sub * 128 < ti.rows; ++sub) {
+                // accumulator row = token row (sub*128 + q*32 + lane), columns = features
+                const uint32_t tacc = tacc0 + (uint32_t)(sub * 256);
+                const int r = sub * 128 + q * 32 + lane;
                 const bool valid = r < ti.rows;
                 const long long orow = ti.out_row + r;
                 if (MODE == kGateUp && C::kEpiBytes > 0) {
                     // h = silu(g) * u, kStgCols columns per staged chunk (see staged_store)
                     uint8_t* stg = smem + C::kEpiOff + q * (32 * C::kStgCols * 2);
-                    const long long row0 = ti.out_row + q * 32;
+                    const long long row0 = ti.out_row + sub * 128 + q * 32;
                     const int fbase = ti.f * 128;
 #pragma unroll 1
                     for (int c0 = 0; c0 < 128; c0 += C::kStgCols) {
@@ -767,7 +783,8 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                         }
                         __syncwarp();
                         staged_store<C::kStgCols>(stg, lane, static_cast<__nv_bfloat16_raw*>(p.out),
-                                                  row0, p.out_ld, fbase + c0, q * 32, ti.rows, p.F);
+                                                  row0, p.out_ld, fbase + c0, sub * 128 + q * 32,
+                                                  ti.rows, p.F);
                         __syncwarp();
                     }
                 } else if (MODE == kGateUp) {
@@ -799,7 +816,7 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                 } else if (MODE == kDown && C::kEpiBytes > 0) {
                     uint8_t* stg = smem + C::kEpiOff + q * (32 * C::kStgCols * 2);
                     const int fbase = ti.f * 256;
-                    const long long row0 = ti.out_row + q * 32;
+                    const long long row0 = ti.out_row + sub * 128 + q * 32;
 #pragma unroll 1
                     for (int c0 = 0; c0 < 256 && fbase + c0 < p.F; c0 += C::kStgCols) {
 #pragma unroll 1
@@ -819,7 +836,8 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                         }
                         __syncwarp();
                         staged_store<C::kStgCols>(stg, lane, static_cast<__nv_bfloat16_raw*>(p.out),
-                                                  row0, p.out_ld, fbase + c0, q * 32, ti.rows, p.F);
+                                                  row0, p.out_ld, fbase + c0, sub * 128 + q * 32,
+                                                  ti.rows, p.F);
                         __syncwarp();
                     }
                 } else {
@@ -861,6 +879,7 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                 }
             } else {
                 // accumulator row = feature (q*32 + lane), columns = tokens
+                const uint32_t tacc = tacc0;
                 const int feat = ti.f * 128 + q * 32 + lane;
                 const bool fvalid = feat < p.F;
 #pragma unroll 1
