@@ -155,6 +155,16 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
     const void* srow = BF16 ? (const void*)(static_cast<const uint16_t*>(a.scores) + row * a.ld)
                             : (const void*)(static_cast<const float*>(a.scores) + row * a.ld);
     constexpr bool cached = CACHED;  // keys of the segment held in shared memory
+    // short rows (one CTA, no window): the radix select's first histogram (the top DBITS bits
+    // of every key) is built while the keys are loaded, which saves a pass over them
+    constexpr bool kFuse0 = !kWin && CACHED;
+    if (kFuse0) {
+        for (int b = tid; b < NB; b += THREADS) hist[b] = 0;
+        __syncthreads();
+    }
+    auto h0 = [&](uint32_t key) {
+        if (kFuse0) atomicAdd(&hist[key >> (32 - DBITS)], 1);
+    };
     if (cached) {
         // one pass over HBM: 16-byte vectors where the row allows, scalars otherwise
         const int per = BF16 ? 8 : 4;
@@ -186,6 +196,7 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
                     hi.w = score_key(__uint_as_float(w[3] & 0xFFFF0000u));
                     reinterpret_cast<uint4*>(keys)[2 * v] = lo;
                     reinterpret_cast<uint4*>(keys)[2 * v + 1] = hi;
+                    h0(lo.x); h0(lo.y); h0(lo.z); h0(lo.w); h0(hi.x); h0(hi.y); h0(hi.z); h0(hi.w);
                 } else {
                     uint4 kq;
                     kq.x = score_key(__uint_as_float(w[0]));
@@ -193,6 +204,7 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
                     kq.z = score_key(__uint_as_float(w[2]));
                     kq.w = score_key(__uint_as_float(w[3]));
                     reinterpret_cast<uint4*>(keys)[v] = kq;
+                    h0(kq.x); h0(kq.y); h0(kq.z); h0(kq.w);
                 }
             }
         }
@@ -211,6 +223,7 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
                 hi.w = score_key(__uint_as_float(w[3] & 0xFFFF0000u));
                 reinterpret_cast<uint4*>(keys)[2 * v] = lo;
                 reinterpret_cast<uint4*>(keys)[2 * v + 1] = hi;
+                h0(lo.x); h0(lo.y); h0(lo.z); h0(lo.w); h0(hi.x); h0(hi.y); h0(hi.z); h0(hi.w);
             } else {
                 uint4 kq;
                 kq.x = score_key(__uint_as_float(w[0]));
@@ -218,9 +231,14 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
                 kq.z = score_key(__uint_as_float(w[2]));
                 kq.w = score_key(__uint_as_float(w[3]));
                 reinterpret_cast<uint4*>(keys)[v] = kq;
+                h0(kq.x); h0(kq.y); h0(kq.z); h0(kq.w);
             }
         }
-        for (int i = nv * per + tid; i < cnt; i += THREADS) keys[i] = load_key<BF16>(srow, j0 + i);
+        for (int i = nv * per + tid; i < cnt; i += THREADS) {
+            const uint32_t key = load_key<BF16>(srow, j0 + i);
+            keys[i] = key;
+            h0(key);
+        }
     }
     __syncthreads();
 
@@ -434,9 +452,12 @@ __global__ void __launch_bounds__(THREADS) indexer_topk_kernel(const TopkArgs a)
             const int top = nbits - dbits * pass;
             const int shift = top > dbits ? top - dbits : 0;
             const int nb = 1 << (top - shift);
-            for (int b = tid; b < nb; b += THREADS) hist[b] = 0;
-            __syncthreads();
-            for (int base = 0; base < rcnt; base += 4 * THREADS) {
+            const bool prebuilt = kFuse0 && pass == 0;  // built during the load
+            if (!prebuilt) {
+                for (int b = tid; b < nb; b += THREADS) hist[b] = 0;
+                __syncthreads();
+            }
+            for (int base = 0; base < rcnt && !prebuilt; base += 4 * THREADS) {
                 const int i = base + 4 * tid;
                 const uint4 q = getr4(i);
                 const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
