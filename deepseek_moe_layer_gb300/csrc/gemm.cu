@@ -870,9 +870,19 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                         } else {
                             float* dst = static_cast<float*>(p.out) + (long long)ti.ks * p.split_stride +
                                          orow * p.out_ld + fbase + c0;
+                            if (fbase + c0 + 32 <= p.F && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                                // whole 16-byte pieces of the row (the scalar form cost the
+                                // prefill router most of its time)
+                                float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (fbase + c0 + i < p.F) dst[i] = __uint_as_float(a[i]);
+                                for (int v = 0; v < 8; ++v)
+                                    d4[v] = make_float4(__uint_as_float(a[4 * v]), __uint_as_float(a[4 * v + 1]),
+                                                        __uint_as_float(a[4 * v + 2]), __uint_as_float(a[4 * v + 3]));
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    if (fbase + c0 + i < p.F) dst[i] = __uint_as_float(a[i]);
+                            }
                         }
                         }
                     }
