@@ -99,6 +99,7 @@ struct Cfg {
             : cmin(12, (216 * 1024 - (kQ ? 2 * kRBytes : 0)) / kStageBytes);
     static constexpr int kRawStages =
         !kQ ? 0 : kTA ? cmin(8, (216 * 1024 - kStages * kStageBytes) / kRBytes) : 2;
+    static constexpr int kRawRing = kRawStages > 0 ? kRawStages : 1;  // for slot arithmetic
     static constexpr int kThreadsCta = kQ ? kThreads + 32 + 32 * kDequantWarps : kThreads;
     static constexpr int kTmemCols = kTA ? 512 : pow2ceil(cmax(32, kAccBufs * kAccCols));
     static constexpr int kN = kSwap ? kTok : 256;
@@ -437,24 +438,25 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                 if (ti.shared) {
                     // normal-mode 4-bit: the operand producer loads the bf16 shared rows;
                     // TMEM-A path: one k-block of them per raw slot (same 128-byte rows)
-                    if (!C::kTA) continue;
-                    for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++rit) {
-                        const int rs = rit % C::kRawStages;
-                        const uint32_t rph = (uint32_t)(rit / C::kRawStages) & 1u;
-                        if (!mbar_wait(&rawempty[rs], rph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
-                        uint8_t* rst = smem + C::kRawOff + rs * C::kRBytes;
-                        mbar_arrive_expect_tx(&rawfull[rs], C::kRBytes);
-                        tma_load_2d(rst, &tm_sw0, &rawfull[rs], kb * kBK, ti.f * C::kFeat, pol_w);
-                        if (MODE == kGateUp)
-                            tma_load_2d(rst + 128 * 128, &tm_sw1, &rawfull[rs], kb * kBK,
-                                        ti.f * C::kFeat, pol_w);
+                    if constexpr (C::kTA) {
+                        for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++rit) {
+                            const int rs = rit % C::kRawRing;
+                            const uint32_t rph = (uint32_t)(rit / C::kRawRing) & 1u;
+                            if (!mbar_wait(&rawempty[rs], rph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
+                            uint8_t* rst = smem + C::kRawOff + rs * C::kRBytes;
+                            mbar_arrive_expect_tx(&rawfull[rs], C::kRBytes);
+                            tma_load_2d(rst, &tm_sw0, &rawfull[rs], kb * kBK, ti.f * C::kFeat, pol_w);
+                            if (MODE == kGateUp)
+                                tma_load_2d(rst + 128 * 128, &tm_sw1, &rawfull[rs], kb * kBK,
+                                            ti.f * C::kFeat, pol_w);
+                        }
                     }
                     continue;
                 }
                 const int wrow = ti.g * p.F + ti.f * C::kFeat;
                 for (int kb = ti.kb0; kb < ti.kb1; kb += C::kRawKB, ++rit) {
-                    const int rs = rit % C::kRawStages;
-                    const uint32_t rph = (uint32_t)(rit / C::kRawStages) & 1u;
+                    const int rs = rit % C::kRawRing;
+                    const uint32_t rph = (uint32_t)(rit / C::kRawRing) & 1u;
                     if (!mbar_wait(&rawempty[rs], rph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
                     uint8_t* rst = smem + C::kRawOff + rs * C::kRBytes;
                     mbar_arrive_expect_tx(&rawfull[rs], C::kRBytes);
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
             }
             if (!ok) {
                 for (int n = (rit > C::kRawStages ? rit - C::kRawStages : 0); n < rit; ++n)
-                    mbar_wait(&rawfull[n % C::kRawStages], (uint32_t)(n / C::kRawStages) & 1u,
+                    mbar_wait(&rawfull[n % C::kRawRing], (uint32_t)(n / C::kRawRing) & 1u,
                               nullptr, 100000000ull);
             }
         }
@@ -618,9 +620,9 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                     // swizzled row segment of kRawKB k-blocks); the slot goes back to the
                     // code producer after its last k-block
                     const int j = (kb - ti.kb0) % C::kRawKB;
-                    const int rs = rit % C::kRawStages;
+                    const int rs = rit % C::kRawRing;
                     if (j == 0) {
-                        const uint32_t rph = (uint32_t)(rit / C::kRawStages) & 1u;
+                        const uint32_t rph = (uint32_t)(rit / C::kRawRing) & 1u;
                         if (!mbar_wait(&rawfull[rs], rph, abort)) { record_timeout(abort); ok = false; break; }
                     }
                     const uint8_t* rrow = smem + C::kRawOff + rs * C::kRBytes + r * 128;
@@ -642,8 +644,8 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                 } else if (C::kTA) {
                     // bf16 shared expert on the TMEM-A path: one k-block per raw slot, the
                     // row's 128 bytes are already the operand
-                    const int rs = rit % C::kRawStages;
-                    const uint32_t rph = (uint32_t)(rit / C::kRawStages) & 1u;
+                    const int rs = rit % C::kRawRing;
+                    const uint32_t rph = (uint32_t)(rit / C::kRawRing) & 1u;
                     if (!mbar_wait(&rawfull[rs], rph, abort)) { record_timeout(abort); ok = false; break; }
                     const uint8_t* rrow = smem + C::kRawOff + rs * C::kRBytes + r * 128;
                     uint4 bw[kWordsPT];
