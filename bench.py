@@ -43,9 +43,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # workload with the hash of the GEMM sources the capture ran; a stale hash reports null.
 # Captures: profiles/moe_gemm_gateup_dsv3_E32_T16.md, moe_gemm_gateup_dsv3_E32_T1024_zipf.md.
 NCU_TRAFFIC = {
-    "dsv3_T128": {"src": "979d74fb5f6797d2", "ratio": (1.705471e9 + 3.342080e6) / 1705541632},
-    "dsv3_T8192_zipf": {"src": "979d74fb5f6797d2",
-                        "ratio": (2.124772e9 + 27.035392e6) / (32 * 2 * 2048 * 7168 * 2
+    "dsv3_T128": {"src": "5bcf3059acb9ebea", "ratio": (1.705460e9 + 3.150080e6) / 1705541632},
+    "dsv3_T8192_zipf": {"src": "5bcf3059acb9ebea",
+                        "ratio": (2.115325e9 + 26.995968e6) / (32 * 2 * 2048 * 7168 * 2
                                                                + 9216 * (7168 + 2048) * 2)},
 }
 
