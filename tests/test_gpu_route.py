@@ -66,6 +66,25 @@ def test_route_exact_ties(E, G, tg, K):
     _run(torch.zeros(3, E, device=DEV), torch.zeros(E, device=DEV), K, G, tg, True, 1.0)
 
 
+def test_route_nan_and_signed_zero():
+    """NaN logits rank below every number (their experts and all-NaN groups are the last
+    choices) and -0 == +0 (sigma(-0) and sigma(+0) tie, the lower expert index first), on
+    both sides (the reading of the gate's comparisons for values the pages leave open)."""
+    g = torch.Generator(device=DEV).manual_seed(12)
+    E = 256
+    logits = torch.randn(300, E, generator=g, device=DEV) * 2
+    logits[::3, ::7] = float("nan")        # scattered NaNs
+    logits[1::3, 32:64] = float("nan")     # a whole group of NaNs
+    logits[2::3, 5] = -0.0
+    logits[2::3, 6] = 0.0
+    logits[2::3, 7:40] = -30.0             # the +-0 pair among the top scores of its rows
+    bias = torch.zeros(E, device=DEV)
+    _run(logits, bias, 8, 8, 4, True, 2.5)
+    _run(logits, bias, 8, 1, 1, False, 1.0)
+    gi, _ = _softmax_check(logits, 8)
+    assert not torch.isnan(logits.gather(1, gi.long())).any()
+
+
 def test_route_bf16_logits_and_leading_dims():
     g = torch.Generator(device=DEV).manual_seed(3)
     logits = torch.randn(4, 33, 256, generator=g, device=DEV).to(torch.bfloat16)
