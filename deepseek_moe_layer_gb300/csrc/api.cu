@@ -261,7 +261,15 @@ int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_
     if (has_shared) dn.ws = {16, sh->down, nullptr, nullptr, nullptr, nullptr, nullptr};
     dn.out = out;
     dn.out_ld = d;
-    dn.max_tiles = mt_bound * ((d + (tok ? 127 : 255)) / (tok ? 128 : 256));
+    // quantised experts: the down GEMM takes its tokens on M at every batch size (256 output
+    // rows per tile and UMMA, half the tiles of the tokens-on-N form over the short I-long
+    // main loop; measured at decode, 4-bit T=32: 0.336 -> 0.272 ms, 8-bit 0.372 -> 0.302 ms,
+    // while the gate/up GEMM stays faster with tokens on N)
+    const int tok_dn = ex->bits != 16 ? 0 : tok;
+    const long long mt_dn = tok_dn == tok ? mt_bound
+                                          : (P + 127) / 128 + E + (has_shared ? (T + 127) / 128 : 0);
+    dn.tok_tile = tok_dn;
+    dn.max_tiles = mt_dn * ((d + (tok_dn ? 127 : 255)) / (tok_dn ? 128 : 256));
     MOE_CUDA(moe::launch_gemm(dn, s), "down GEMM");
     MOE_CUDA(phase(6, s), "phase event");
     return MOE_OK;
