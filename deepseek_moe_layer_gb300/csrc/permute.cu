@@ -39,10 +39,14 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
     const long long c1 = min(P, c0 + chunk);
     int32_t* my = hist + warp * E;
 
-    // pass 1: per-warp histogram
-    for (long long p = c0 + lane; p < c1; p += 32) {
-        const int e = inds[p];
-        if (e >= 0 && e < E) atomicAdd(&my[e], 1);
+    // pass 1: per-warp histogram (four loads in flight per lane)
+    for (long long p0 = c0 + lane; p0 < c1; p0 += 128) {
+        int ev[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ev[u] = p0 + 32 * u < c1 ? __ldg(inds + p0 + 32 * u) : -1;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (ev[u] >= 0 && ev[u] < E) atomicAdd(&my[ev[u]], 1);
     }
     __syncthreads();
 
@@ -89,12 +93,25 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
     if (threadIdx.x == blockDim.x - 1) offsets[E] = wsum[31];
     __syncthreads();
 
-    // pass 3: stable placement
+    // pass 3: stable placement, 32 pairs a step in pair order (the next three steps' expert
+    // ids already in flight)
     const unsigned lt_mask = (1u << lane) - 1u;
+    int ahead[3];
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+        const long long q = c0 + 32 * (u + 1) + lane;
+        ahead[u] = q < c1 ? __ldg(inds + q) : -1;
+    }
+    int cur = c0 + lane < c1 ? __ldg(inds + c0 + lane) : -1;
     for (long long base = c0; base < c1; base += 32) {
         const long long p = base + lane;
         const bool active = p < c1;
-        const int e = active ? inds[p] : -1;
+        const int e = active ? cur : -1;
+        cur = ahead[0];
+        ahead[0] = ahead[1];
+        ahead[1] = ahead[2];
+        const long long q = base + 128 + lane;
+        ahead[2] = q < c1 ? __ldg(inds + q) : -1;
         const bool valid = active && e >= 0 && e < E;
         const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1 - lane);
         int pos = 0;
