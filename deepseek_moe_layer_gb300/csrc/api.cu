@@ -388,7 +388,10 @@ int forward_impl(const moe_layer_args_t& A, void* ws, size_t ws_bytes, cudaStrea
     MOE_CUDA(phase(2, s), "phase event");
 
     // a3: dispatch
-    MOE_CUDA(moe::launch_permute(inds, P, E, counts, offsets, perm, inv, s), "permute kernel");
+    // (the expert-output buffer, written only by the down GEMM, is the dispatch's scratch)
+    MOE_CUDA(moe::launch_permute(inds, P, E, counts, offsets, perm, inv, s, eo,
+                                 (size_t)(P + (has_shared ? T : 0)) * d * 2),
+             "permute kernel");
     MOE_CUDA(phase(3, s), "phase event");
 
     // a4 + a5 (+ a7): expert SwiGLU GEMMs, shared expert as the last group

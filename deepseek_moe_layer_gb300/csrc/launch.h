@@ -32,7 +32,12 @@ cudaError_t launch_add_offset(float* logits, long long T, int E, const float* of
 
 // ---- dispatch -----------------------------------------------------------------------
 cudaError_t launch_permute(const int32_t* inds, long long P, int E, int32_t* counts,
-                           int32_t* offsets, int32_t* perm, int32_t* inv, cudaStream_t s);
+                           int32_t* offsets, int32_t* perm, int32_t* inv, cudaStream_t s,
+                           void* scratch = nullptr, size_t scratch_bytes = 0);
+// scratch (optional, device): with at least permute_scratch_bytes(E) bytes, batches of at
+// least kPermMultiMin pairs are dispatched by many CTAs instead of one.
+constexpr long long kPermMultiMin = 8192;
+size_t permute_scratch_bytes(int E);
 // x_perm[j] = x[perm[j] / K] for the dispatched slots j < offsets[E].
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t* offsets, int E,
                                int K, long long P, int d, void* x_perm, cudaStream_t s);

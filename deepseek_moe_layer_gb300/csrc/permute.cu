@@ -128,6 +128,126 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
     }
 }
 
+// ---- large batches: the same dispatch spread over kPermCtas CTAs ----
+// CTA b owns the contiguous chunk b of the pairs.  permute_count_kernel writes the chunk's
+// expert counts cnt[b][e]; permute_place_kernel turns the count matrix into this chunk's
+// slot base per expert (the slots of expert e: chunks in order, inside a chunk warps in
+// order, inside a warp pairs in order: the same stable order as the one-CTA kernel), then
+// places its chunk as that kernel does.  The scattered slot stores are spread over many SMs
+// (from one SM they set the pace of the one-CTA kernel at large batches).
+constexpr int kPermCtas = 64;
+
+__global__ void __launch_bounds__(1024) permute_count_kernel(const int32_t* __restrict__ inds,
+                                                             long long P, int E, long long chunk,
+                                                             int32_t* __restrict__ cnt) {
+    extern __shared__ int32_t sh[];  // [E]
+    for (int i = threadIdx.x; i < E; i += blockDim.x) sh[i] = 0;
+    __syncthreads();
+    const long long c0 = min(P, (long long)blockIdx.x * chunk);
+    const long long c1 = min(P, c0 + chunk);
+    for (long long p = c0 + threadIdx.x; p < c1; p += blockDim.x) {
+        const int e = __ldg(inds + p);
+        if (e >= 0 && e < E) atomicAdd(&sh[e], 1);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[(long long)blockIdx.x * E + i] = sh[i];
+}
+
+__global__ void __launch_bounds__(1024) permute_place_kernel(
+    const int32_t* __restrict__ inds, long long P, int E, long long chunk,
+    const int32_t* __restrict__ cnt, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    extern __shared__ int32_t sh[];
+    int32_t* hist = sh;                      // [kPermWarps][E]
+    int32_t* wsum = sh + kPermWarps * E;     // [32] scan carries
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x, nb = gridDim.x;
+
+    for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) hist[i] = 0;
+    // expert e (thread e, E <= 1024): its pairs in all chunks and in the chunks before b
+    const int e_t = threadIdx.x;
+    int tot = 0, pre = 0;
+    if (e_t < E)
+        for (int c = 0; c < nb; ++c) {
+            const int v = __ldg(cnt + (long long)c * E + e_t);
+            tot += v;
+            pre += c < b ? v : 0;
+        }
+    // exclusive scan of the totals over the experts
+    int incl = tot;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = wsum[lane];
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xFFFFFFFFu, v, off);
+            if (lane >= off) v += u;
+        }
+        wsum[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    const int off_e = (warp > 0 ? wsum[warp - 1] : 0) + incl - tot;  // slot of expert e's first pair
+    if (b == 0) {
+        if (e_t < E) {
+            counts[e_t] = tot;
+            offsets[e_t] = off_e;
+        }
+        if (threadIdx.x == blockDim.x - 1) offsets[E] = wsum[31];
+    }
+
+    // this chunk's per-warp histograms
+    const long long c0 = min(P, (long long)b * chunk);
+    const long long c1 = min(P, c0 + chunk);
+    const long long wch = (c1 - c0 + kPermWarps - 1) / kPermWarps;
+    const long long w0 = min(c1, c0 + (long long)warp * wch);
+    const long long w1 = min(c1, w0 + wch);
+    int32_t* my = hist + warp * E;
+    for (long long p0 = w0 + lane; p0 < w1; p0 += 128) {
+        int ev[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ev[u] = p0 + 32 * u < w1 ? __ldg(inds + p0 + 32 * u) : -1;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (ev[u] >= 0 && ev[u] < E) atomicAdd(&my[ev[u]], 1);
+    }
+    __syncthreads();
+    // per-(warp, expert) slot bases
+    if (e_t < E) {
+        int run = off_e + pre;
+        for (int w = 0; w < kPermWarps; ++w) {
+            const int h = hist[w * E + e_t];
+            hist[w * E + e_t] = run;
+            run += h;
+        }
+    }
+    __syncthreads();
+
+    // stable placement of the warp's pairs, 32 a step in pair order
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (long long base = w0; base < w1; base += 32) {
+        const long long p = base + lane;
+        const bool active = p < w1;
+        const int e = active ? __ldg(inds + p) : -1;
+        const bool valid = active && e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1 - lane);
+        int pos = 0;
+        if (valid) pos = my[e] + __popc(peers & lt_mask);
+        __syncwarp();
+        if (valid && (__ffs(peers) - 1) == lane) my[e] += __popc(peers);
+        __syncwarp();
+        if (valid) {
+            perm[pos] = (int32_t)p;
+            inv[p] = pos;
+        } else if (active) {
+            inv[p] = -1;
+        }
+    }
+}
+
 // One warp per dispatched slot: x_perm[j] = x[perm[j] / K], 16-byte vectors.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
                                                           const int32_t* __restrict__ perm,
@@ -156,16 +276,31 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 
 }  // namespace
 
+size_t permute_scratch_bytes(int E) { return sizeof(int32_t) * (size_t)kPermCtas * E; }
+
 cudaError_t launch_permute(const int32_t* inds, long long P, int E, int32_t* counts,
-                           int32_t* offsets, int32_t* perm, int32_t* inv, cudaStream_t s) {
+                           int32_t* offsets, int32_t* perm, int32_t* inv, cudaStream_t s,
+                           void* scratch, size_t scratch_bytes) {
     const size_t smem = sizeof(int32_t) * ((size_t)kPermWarps * E + 32);
     static bool attr_done = false;
     if (!attr_done) {
+        const int most = (int)(sizeof(int32_t) * (kPermWarps * 1024 + 32));
         cudaError_t err = cudaFuncSetAttribute(permute_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)(sizeof(int32_t) * (kPermWarps * 1024 + 32)));
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(permute_place_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, most);
         if (err != cudaSuccess) return err;
         attr_done = true;
+    }
+    if (P >= kPermMultiMin && scratch && scratch_bytes >= permute_scratch_bytes(E)) {
+        const long long chunk = (P + kPermCtas - 1) / kPermCtas;
+        int32_t* cnt = static_cast<int32_t*>(scratch);
+        permute_count_kernel<<<kPermCtas, 1024, sizeof(int32_t) * (size_t)E, s>>>(inds, P, E,
+                                                                                   chunk, cnt);
+        permute_place_kernel<<<kPermCtas, 1024, smem, s>>>(inds, P, E, chunk, cnt, counts,
+                                                           offsets, perm, inv);
+        return cudaGetLastError();
     }
     permute_kernel<<<1, 1024, smem, s>>>(inds, P, E, counts, offsets, perm, inv);
     return cudaGetLastError();

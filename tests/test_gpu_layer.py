@@ -70,8 +70,8 @@ def test_tiny_layer_all_tokens():
 
 # T values that take each token-tile choice of the expert GEMMs (16/32/64 tokens on N,
 # 128-token tiles on M) and of the router (tokens on N up to 256, on M above), with
-# ragged tails everywhere.
-@pytest.mark.parametrize("T", [1, 5, 33, 96, 150, 300, 520])
+# ragged tails everywhere; from 2048 tokens (8192 pairs) the dispatch runs over many CTAs.
+@pytest.mark.parametrize("T", [1, 5, 33, 96, 150, 300, 520, 2048, 2501])
 def test_layer_token_tiles(T):
     w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=T)
     _check_forward(w, inputs.gen_layer(w, DEV, seed=T))
