@@ -306,8 +306,10 @@ def time_layer(w, data, steps, warmup, dev, sampler=None, flush_l2=False):
     _, inds, _, _ = layer(x, want_intermediates=True)
     torch.cuda.synchronize(dev)
     counts = np.bincount(inds.cpu().numpy().reshape(-1), minlength=w.E)
+    # seven kernels per forward; from 8192 token-expert pairs the dispatch is two launches
+    per_fwd = 7 + (1 if w.T * w.top_k >= 8192 else 0)
     return dict(total_ms=float(per_step.sum()), ms=float(per_step.mean()), phases=phases,
-                counts=counts, launches=7 * steps)
+                counts=counts, launches=per_fwd * steps)
 
 
 def time_e2e(w, data, steps, warmup, dev):
