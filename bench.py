@@ -41,13 +41,43 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # workloads are too large to replay); traffic grows with the expert bytes processed, so the
 # per-launch traffic of the full workload is ratio x its algorithmic bytes.  Keyed by
 # workload with the hash of the GEMM sources the capture ran; a stale hash reports null.
-# Captures: profiles/moe_gemm_gateup_dsv3_E32_T16.md, moe_gemm_gateup_dsv3_E32_T1024_zipf.md.
 NCU_TRAFFIC = {
     "dsv3_T128": {"src": "5bcf3059acb9ebea", "ratio": (1.705460e9 + 3.150080e6) / 1705541632},
     "dsv3_T8192_zipf": {"src": "5bcf3059acb9ebea",
                         "ratio": (2.115325e9 + 26.995968e6) / (32 * 2 * 2048 * 7168 * 2
                                                                + 9216 * (7168 + 2048) * 2)},
 }
+
+
+NEAR_TIE = 1e-6
+
+
+def near_tie_count(logits, bias, top_k, n_group, topk_group):
+    """Rows of fp32 router logits [rows, E] whose K-th and (K+1)-th biased scores, or whose
+    topk_group-th and next group scores, differ by a nonzero amount under 1e-6: two fp32
+    sigmoid implementations (device expf, host libm) may order such candidates differently,
+    so the parity rules count them and leave them out of the bit-exact verdict.  Evaluated
+    in float64 on the host from the device's own logits."""
+    lg = np.asarray(logits, np.float32).astype(np.float64)
+    b = 1.0 / (1.0 + np.exp(-lg)) + np.asarray(bias, np.float32).astype(np.float64)[None, :]
+    rows, E = b.shape
+    flag = np.zeros(rows, bool)
+    if n_group > 1 and n_group - topk_group > 0:
+        eg = E // n_group
+        srt = np.sort(b.reshape(rows, n_group, eg), axis=2)
+        gs = srt[:, :, -1] + srt[:, :, -2]
+        order = np.sort(gs, axis=1)[:, ::-1]
+        gap = order[:, topk_group - 1] - order[:, topk_group]
+        flag |= (gap > 0) & (gap < NEAR_TIE)
+        keep = np.zeros_like(gs, bool)
+        np.put_along_axis(keep, np.argsort(-gs, axis=1, kind="stable")[:, :topk_group], True,
+                          axis=1)
+        b = np.where(np.repeat(keep, eg, axis=1), b, 0.0)
+    if top_k < E:
+        srt = np.sort(b, axis=1)[:, ::-1]
+        gap = srt[:, top_k - 1] - srt[:, top_k]
+        flag |= (gap > 0) & (gap < NEAR_TIE)
+    return int(flag.sum())
 
 
 def kernel_source_hash():
@@ -217,9 +247,12 @@ def time_routing(dev, replays=50):
         stream.synchronize()
         us = a.elapsed_time(z) * 1e3 / (replays * nbuf)
         nbytes = rows * E * 4 + rows * K * 8
+        rf = roofline("hbm", nbytes / (us * 1e-6), load_peaks()[0], False)
         out[name] = {"us_per_launch": round(us, 3), "rows_per_s": round(rows / (us * 1e-6), 1),
-                     "bytes": nbytes, "launches": replays * nbuf,
-                     "roofline": roofline("hbm", nbytes / (us * 1e-6), load_peaks()[0], False)}
+                     "bytes": nbytes, "launches": replays * nbuf, "roofline": rf,
+                     "roofline_frac": rf["frac"],
+                     "near_ties": near_tie_count(logits.cpu().numpy(), bias.cpu().numpy(), K,
+                                                 p["n_group"], p["topk_group"])}
     del bufs
     torch.cuda.empty_cache()
     return {"workload": f"routing_{rows}x{E}", "l2": "16 rotating copies of the logits "
@@ -303,13 +336,15 @@ def time_layer(w, data, steps, warmup, dev, sampler=None, flush_l2=False):
     per_step = np.array([evs[s][0].elapsed_time(evs[s][7]) for s in range(steps)])
     phases = {name: float(np.mean([evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)]))
               for i, name in enumerate(binding.PHASES)}
-    _, inds, _, _ = layer(x, want_intermediates=True)
+    _, inds, _, logits = layer(x, want_intermediates=True)
     torch.cuda.synchronize(dev)
     counts = np.bincount(inds.cpu().numpy().reshape(-1), minlength=w.E)
+    ties = near_tie_count(logits.cpu().numpy(), data["bias"].cpu().numpy(), w.top_k, w.n_group,
+                          w.topk_group)
     # seven kernels per forward; from 8192 token-expert pairs the dispatch is two launches
     per_fwd = 7 + (1 if w.T * w.top_k >= 8192 else 0)
     return dict(total_ms=float(per_step.sum()), ms=float(per_step.mean()), phases=phases,
-                counts=counts, launches=per_fwd * steps)
+                counts=counts, launches=per_fwd * steps, near_ties=ties)
 
 
 def time_e2e(w, data, steps, warmup, dev):
@@ -449,11 +484,14 @@ def cpu_baseline(w, data, target_s=10.0):
 # ---------------------------------------------------------------------------------------
 
 def workload_data(name, dev, base=None):
+    """Inputs of a layer workload; with `base`, its weights are reused (same shapes and
+    width) and only the tokens, the bias and the logit offsets are drawn for `name`."""
     w = inputs.WORKLOADS[name]
     if base is None:
         return w, inputs.gen_layer(w, dev, seed=0)
     data = dict(base)
     data["x"] = inputs.gen_tokens(w, dev, seed=0)
+    data["bias"] = inputs.gen_bias(w, dev, seed=0)
     data["logit_offset"] = inputs.zipf_offsets(w.E, dev, 0) if w.zipf else None
     return w, data
 
@@ -481,38 +519,69 @@ def run_ours(args):
     e2e = time_e2e(w, data, args.steps, args.warmup, dev)
     alg = algorithmic(w, t["counts"])
 
-    def summary(wx, tx):
+    base_cpu = rank == 0 and ws == 1 and not args.no_cpu_baseline
+
+    def summary(wx, tx, dx=None):
+        """One workload's line.  Besides the nested roofline objects it carries their
+        figures as plain numbers (a parser that keeps scalars only still sees them), the
+        near-tie count of its routing, and, on rank 0 of a single-GPU run, the CPU oracle
+        timed on a bounded sample of the same workload."""
         algx = algorithmic(wx, tx["counts"])
-        return {"workload": wx.name, "T": wx.T, "expert_bits": wx.bits,
-                "value": round(wx.T / (tx["ms"] / 1e3), 1),
-                "unit": "tokens/s", "ms_per_step": round(tx["ms"], 4),
-                "phases_ms": {k: round(v, 4) for k, v in tx["phases"].items()},
-                "experts_hit": algx["experts_hit"], "max_expert_load": int(tx["counts"].max()),
-                "roofline": kernel_roofline(wx, tx, algx, peaks, src),
-                "layer_roofline": layer_roofline(algx, tx["ms"], peaks)}
+        kr = kernel_roofline(wx, tx, algx, peaks, src)
+        lr = layer_roofline(algx, tx["ms"], peaks)
+        out = {"workload": wx.name, "T": wx.T, "expert_bits": wx.bits,
+               "value": round(wx.T / (tx["ms"] / 1e3), 1),
+               "unit": "tokens/s", "ms_per_step": round(tx["ms"], 4),
+               "experts_hit": algx["experts_hit"], "max_expert_load": int(tx["counts"].max()),
+               "near_ties": tx["near_ties"],
+               "roofline_bound": kr["bound"], "roofline_achieved": kr["achieved"],
+               "roofline_peak": kr["peak"], "roofline_unit": kr["unit"],
+               "roofline_frac": kr["frac"], "roofline_traffic": kr["traffic"],
+               "gate_up_ms": kr["ms"], "layer_roofline_frac": lr["frac"],
+               "layer_roofline_achieved": lr["achieved"], "layer_roofline_unit": lr["unit"],
+               "phases_ms": {k: round(v, 4) for k, v in tx["phases"].items()},
+               "roofline": kr, "layer_roofline": lr}
+        if dx is not None and base_cpu:
+            cb = cpu_baseline(wx, dx, target_s=4.0)
+            out["cpu_baseline"] = cb
+            out["cpu_baseline_tokens_per_s"] = cb["value"]
+        return out
 
     pre = None
     if do_pre:
-        pre = summary(wp, tp)
+        pre = summary(wp, tp, dp)
         del dp
+    # the same decode layer under near-uniform routing (bias at standard deviation 0.05):
+    # the expert stream a uniform router touches
+    uni = None
+    if args.uniform and w.name == "dsv3_T128":
+        wu, du = workload_data("dsv3_T128_uniform", dev, base=data)
+        tu = time_layer(wu, du, args.steps, args.warmup, dev, flush_l2=args.l2_flush)
+        uni = summary(wu, tu)
+        del du
     # the affine 4-bit expert workloads (decode T=32, prefill T=4096 with Zipf routing)
     q4 = {}
     if args.q4 and w.d == 7168 and w.E == 256:
         wq, dq = workload_data("dsv3_q4_T32", dev)
         tq = time_layer(wq, dq, args.steps, args.warmup, dev, flush_l2=args.l2_flush)
-        q4["q4_decode"] = summary(wq, tq)
+        q4["q4_decode"] = summary(wq, tq, dq)
+        if args.uniform:
+            wqu, dqu = workload_data("dsv3_q4_T32_uniform", dev, base=dq)
+            tqu = time_layer(wqu, dqu, args.steps, args.warmup, dev, flush_l2=args.l2_flush)
+            q4["q4_decode_uniform"] = summary(wqu, tqu)
+            del dqu
         wq2, dq2 = workload_data("dsv3_q4_T4096_zipf", dev, base=dq)
         tq2 = time_layer(wq2, dq2, args.steps, args.warmup, dev, flush_l2=args.l2_flush)
-        q4["q4_prefill"] = summary(wq2, tq2)
+        q4["q4_prefill"] = summary(wq2, tq2, dq2)
         del dq, dq2
         torch.cuda.empty_cache()
     if args.q8 and w.d == 7168 and w.E == 256:
         wq, dq = workload_data("dsv3_q8_T32", dev)
         tq = time_layer(wq, dq, args.steps, args.warmup, dev, flush_l2=args.l2_flush)
-        q4["q8_decode"] = summary(wq, tq)
+        q4["q8_decode"] = summary(wq, tq, dq)
         wq2, dq2 = workload_data("dsv3_q8_T4096_zipf", dev, base=dq)
         tq2 = time_layer(wq2, dq2, args.steps, args.warmup, dev, flush_l2=args.l2_flush)
-        q4["q8_prefill"] = summary(wq2, tq2)
+        q4["q8_prefill"] = summary(wq2, tq2, dq2)
         del dq, dq2
         torch.cuda.empty_cache()
 
@@ -540,6 +609,7 @@ def run_ours(args):
         "peaks_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
         "phases_ms": {k: round(v, 4) for k, v in t["phases"].items()},
         "experts_hit": alg["experts_hit"],
+        "near_ties": t["near_ties"],
         "clocks": clocks,
         "e2e": {"value": round(ws * args.steps * w.T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
@@ -548,6 +618,8 @@ def run_ours(args):
     }
     if pre is not None:
         line["prefill"] = pre
+    if uni is not None:
+        line["decode_uniform"] = uni
     line.update(q4)
     if routing is not None:
         line["routing"] = routing
@@ -615,6 +687,8 @@ def main():
                     help="skip the DSA indexer selection workloads")
     ap.add_argument("--no-q4", dest="q4", action="store_false",
                     help="skip the affine 4-bit expert workloads")
+    ap.add_argument("--no-uniform", dest="uniform", action="store_false",
+                    help="skip the near-uniform-routing decode workloads")
     args = ap.parse_args()
     if args.prefill in ("", "none"):
         args.prefill = None

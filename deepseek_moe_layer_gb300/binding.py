@@ -25,7 +25,8 @@ EXPORTS = ("moe_last_error", "moe_version", "moe_device_status", "moe_route_deep
            "moe_grouped_swiglu_workspace_bytes", "moe_combine", "moe_forward",
            "moe_forward_workspace_bytes", "moe_set_phase_events", "moe_forward_noalloc",
            "moe_route_softmax", "moe_shared_gate", "moe_combine_gated", "moe_forward_ex",
-           "moe_forward_ex_workspace_bytes", "moe_watchdog_selftest", "moe_indexer_topk")
+           "moe_forward_ex_workspace_bytes", "moe_watchdog_selftest", "moe_indexer_topk",
+           "moe_set_fault", "moe_get_fault")
 MOE_ROUTE_DEEPSEEK, MOE_ROUTE_SOFTMAX = 0, 1
 
 
@@ -105,11 +106,14 @@ def lib(path: str | None = None):
             L.moe_forward_ex_workspace_bytes.restype = sz
             L.moe_watchdog_selftest.argtypes = [i64, P]
             L.moe_indexer_topk.argtypes = [P, ctypes.c_int, i64, i32, i64, P, i32, P, P, i64, P]
+            L.moe_set_fault.argtypes = [i32, i32]
+            L.moe_get_fault.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(i32)]
             for name in ("moe_device_status", "moe_route_deepseek", "moe_permute",
                          "moe_router_logits", "moe_grouped_swiglu", "moe_combine",
                          "moe_forward", "moe_set_phase_events", "moe_forward_noalloc",
                          "moe_route_softmax", "moe_shared_gate", "moe_combine_gated",
-                         "moe_forward_ex", "moe_watchdog_selftest", "moe_indexer_topk"):
+                         "moe_forward_ex", "moe_watchdog_selftest", "moe_indexer_topk",
+                         "moe_set_fault", "moe_get_fault"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -449,3 +453,19 @@ def watchdog_selftest(limit_ns=20_000_000, stream=None):
     """Launches a wait that nothing completes, bounded by limit_ns; afterwards
     device_status() raises MoeError(MOE_ERR_TIMEOUT)."""
     _check(lib().moe_watchdog_selftest(int(limit_ns), _stream(stream)))
+
+
+MOE_FAULT_NONE, MOE_FAULT_LAUNCH = 0, 1
+
+
+def set_fault(kind=MOE_FAULT_NONE, at=0):
+    """Test hook: with MOE_FAULT_LAUNCH the at-th kernel launch of every later call reports
+    MOE_ERR_CUDA instead of launching; MOE_FAULT_NONE turns it off."""
+    _check(lib().moe_set_fault(int(kind), int(at)))
+
+
+def get_fault():
+    """(kind, at) of the fault hook (MOE_FAULT in the environment sets the initial state)."""
+    k, a = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().moe_get_fault(ctypes.byref(k), ctypes.byref(a)))
+    return k.value, a.value

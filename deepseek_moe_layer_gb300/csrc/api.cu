@@ -8,8 +8,11 @@
 // unchanged on failure) and "Findings" L1/L2 with the author's reply (the validation
 // matrix: null arguments, top_k == 0, top_k > E, E % n_group != 0, topk_group out of
 // [1, n_group], n_group > 1 with fewer than two experts per group, bias rank != 1).
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <string>
 
 #include "../../include/moe_gb300.h"
@@ -44,6 +47,53 @@ int cuda_fail(cudaError_t e, const char* where) {
         if (e_ != cudaSuccess) return cuda_fail(e_, where); \
     } while (0)
 
+// Host-side fault injection (a test hook; off unless MOE_FAULT is set in the environment or
+// moe_set_fault() is called).  MOE_FAULT=launch[:N] makes the N-th kernel launch (0-based,
+// default 0) of every API call report MOE_ERR_CUDA instead of launching, so the error path
+// after earlier launches can be exercised without making a GPU fail.  The launch count
+// restarts at every entry point.
+std::atomic<int> g_fault_kind{-1};  // -1: environment not read yet
+std::atomic<int> g_fault_at{0};
+thread_local int g_launch_no = 0;
+
+void fault_init() {
+    int expected = -1;
+    if (g_fault_kind.load(std::memory_order_acquire) != -1) return;
+    int kind = MOE_FAULT_NONE, at = 0;
+    const char* env = getenv("MOE_FAULT");
+    if (env && strncmp(env, "launch", 6) == 0 && (env[6] == '\0' || env[6] == ':')) {
+        kind = MOE_FAULT_LAUNCH;
+        at = env[6] == ':' ? atoi(env + 7) : 0;
+        if (at < 0) at = 0;
+    }
+    g_fault_at.store(at, std::memory_order_relaxed);
+    g_fault_kind.compare_exchange_strong(expected, kind, std::memory_order_acq_rel);
+}
+
+// True when the launch about to be made is the one the hook fails.
+bool fault_this_launch() {
+    fault_init();
+    const int n = g_launch_no++;
+    return g_fault_kind.load(std::memory_order_acquire) == MOE_FAULT_LAUNCH &&
+           n == g_fault_at.load(std::memory_order_relaxed);
+}
+
+// Start of an entry point: clears the thread's error text and restarts its launch count.
+void begin_call() {
+    g_err.clear();
+    g_launch_no = 0;
+}
+
+// A kernel launch through one of the launchers: MOE_ERR_CUDA on a failed launch, or when
+// the fault hook selects it (then nothing is launched).
+#define MOE_LAUNCH(call, where)                                                        \
+    do {                                                                               \
+        if (fault_this_launch())                                                       \
+            return fail(MOE_ERR_CUDA, "%s: injected launch fault (MOE_FAULT)", where); \
+        cudaError_t e_ = (call);                                                       \
+        if (e_ != cudaSuccess) return cuda_fail(e_, where);                            \
+    } while (0)
+
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxPhaseEvents = 8;
 
@@ -65,15 +115,15 @@ int check_device() {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(MOE_ERR_NODEVICE, "no CUDA device: %s", cudaGetErrorString(e));
-    static int checked[64] = {0};
-    if (dev >= 0 && dev < 64 && checked[dev] == 1) return MOE_OK;
+    static std::atomic<int> checked[64] = {};
+    if (dev >= 0 && dev < 64 && checked[dev].load(std::memory_order_acquire) == 1) return MOE_OK;
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (major != 10 || minor != 3)
         return fail(MOE_ERR_NODEVICE, "device %d is sm_%d%d; this library is built for sm_103a",
                     dev, major, minor);
-    if (dev >= 0 && dev < 64) checked[dev] = 1;
+    if (dev >= 0 && dev < 64) checked[dev].store(1, std::memory_order_release);
     return MOE_OK;
 }
 
@@ -207,8 +257,9 @@ ForwardWs forward_ws(int64_t T, int32_t d, int32_t I, int32_t E, int32_t K, int 
 }
 
 // Maximum K-split of the router over every device plan (the workspace must not depend on
-// the device it is sized on): d/64 k-blocks at most.
-int router_ksplit_bound(int32_t d) { return d / 64; }
+// the device it is sized on): router_plan keeps at least 8 of the d/64 k-blocks per split,
+// so no plan splits more than d/512 ways.
+int router_ksplit_bound(int32_t d) { return d / 512 > 1 ? d / 512 : 1; }
 
 int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_t K,
                const int32_t* offsets, const int32_t* perm, const moe_expert_weights_t* ex,
@@ -218,7 +269,7 @@ int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_
     void* x_perm = ws + lw.x_perm;
     void* h = ws + lw.h;
     const int has_shared = sh != nullptr;
-    MOE_CUDA(moe::launch_gather_rows(x, perm, offsets, E, K, P, d, x_perm, s), "gather rows");
+    MOE_LAUNCH(moe::launch_gather_rows(x, perm, offsets, E, K, P, d, x_perm, s), "gather rows");
     MOE_CUDA(phase(4, s), "phase event");
     const int tok = expert_tok_tile(P, E, ex->bits);
     const int tokn = tok ? tok : 128;
@@ -245,7 +296,7 @@ int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_
     g.out_ld = I;
     g.tok_tile = tok;
     g.max_tiles = mt_bound * (I / 128);
-    MOE_CUDA(moe::launch_gemm(g, s), "gate/up GEMM");
+    MOE_LAUNCH(moe::launch_gemm(g, s), "gate/up GEMM");
     MOE_CUDA(phase(5, s), "phase event");
 
     moe::GemmArgs dn = g;
@@ -270,7 +321,7 @@ int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_
                                           : (P + 127) / 128 + E + (has_shared ? (T + 127) / 128 : 0);
     dn.tok_tile = tok_dn;
     dn.max_tiles = mt_dn * ((d + (tok_dn ? 127 : 255)) / (tok_dn ? 128 : 256));
-    MOE_CUDA(moe::launch_gemm(dn, s), "down GEMM");
+    MOE_LAUNCH(moe::launch_gemm(dn, s), "down GEMM");
     MOE_CUDA(phase(6, s), "phase event");
     return MOE_OK;
 }
@@ -362,7 +413,7 @@ int forward_impl(const moe_layer_args_t& A, void* ws, size_t ws_bytes, cudaStrea
     g.out_ld = E;
     g.tok_tile = rp.tok_tile;
     g.max_tiles = rp.tiles;
-    MOE_CUDA(moe::launch_gemm(g, s), "router GEMM");
+    MOE_LAUNCH(moe::launch_gemm(g, s), "router GEMM");
     MOE_CUDA(phase(1, s), "phase event");
 
     // a2: gate (sums the partials in split order, adds the offset)
@@ -384,12 +435,12 @@ int forward_impl(const moe_layer_args_t& A, void* ws, size_t ws_bytes, cudaStrea
     ra.scores = scores;
     ra.logits_out = A.logits_out;
     ra.softmax = softmax ? 1 : 0;
-    MOE_CUDA(moe::launch_route(ra, s), "route kernel");
+    MOE_LAUNCH(moe::launch_route(ra, s), "route kernel");
     MOE_CUDA(phase(2, s), "phase event");
 
     // a3: dispatch
     // (the expert-output buffer, written only by the down GEMM, is the dispatch's scratch)
-    MOE_CUDA(moe::launch_permute(inds, P, E, counts, offsets, perm, inv, s, eo,
+    MOE_LAUNCH(moe::launch_permute(inds, P, E, counts, offsets, perm, inv, s, eo,
                                  (size_t)(P + (has_shared ? T : 0)) * d * 2),
              "permute kernel");
     MOE_CUDA(phase(3, s), "phase event");
@@ -401,11 +452,11 @@ int forward_impl(const moe_layer_args_t& A, void* ws, size_t ws_bytes, cudaStrea
 
     // a6: combine (the gated shared expert weighs its row by sigmoid(x . w_shared_gate))
     if (sgate)
-        MOE_CUDA(moe::launch_shared_gate(A.x, T, d, A.w_shared_gate, sgate, s), "shared gate");
+        MOE_LAUNCH(moe::launch_shared_gate(A.x, T, d, A.w_shared_gate, sgate, s), "shared gate");
     const void* so = has_shared ? static_cast<const void*>(static_cast<const uint8_t*>(eo) +
                                                            (size_t)P * d * 2)
                                 : nullptr;
-    MOE_CUDA(moe::launch_combine(eo, scores, inv, so, T, K, d, A.y, s, sgate), "combine kernel");
+    MOE_LAUNCH(moe::launch_combine(eo, scores, inv, so, T, K, d, A.y, s, sgate), "combine kernel");
     MOE_CUDA(phase(7, s), "phase event");
     return MOE_OK;
 }
@@ -435,7 +486,7 @@ int moe_device_status(int32_t clear, moe_stream_t stream) {
 int moe_indexer_topk(const void* scores, moe_dtype_t dtype, int64_t rows, int32_t n,
                      int64_t ld, const int32_t* lengths, int32_t k, int32_t* inds,
                      uint8_t* mask, int64_t mask_ld, moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(dtype == MOE_DTYPE_F32 || dtype == MOE_DTYPE_BF16, "dtype %d unknown", (int)dtype);
     MOE_CHECK(rows >= 0, "rows = %lld < 0", (long long)rows);
     MOE_CHECK(n >= 0, "n = %d < 0", n);
@@ -458,17 +509,17 @@ int moe_indexer_topk(const void* scores, moe_dtype_t dtype, int64_t rows, int32_
     a.mask = mask;
     a.mask_ld = mask_ld;
     moe::indexer_topk_plan(a);
-    MOE_CUDA(moe::launch_indexer_topk(a, (cudaStream_t)stream), "indexer top-k kernel");
+    MOE_LAUNCH(moe::launch_indexer_topk(a, (cudaStream_t)stream), "indexer top-k kernel");
     return MOE_OK;
 }
 
 int moe_watchdog_selftest(int64_t limit_ns, moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(limit_ns >= 1000 && limit_ns <= 1000000000, "limit_ns = %lld outside [1e3, 1e9]",
               (long long)limit_ns);
     int rc = check_device();
     if (rc) return rc;
-    MOE_CUDA(moe::launch_watchdog_selftest((unsigned long long)limit_ns, (cudaStream_t)stream),
+    MOE_LAUNCH(moe::launch_watchdog_selftest((unsigned long long)limit_ns, (cudaStream_t)stream),
              "watchdog self-test kernel");
     return MOE_OK;
 }
@@ -476,7 +527,7 @@ int moe_watchdog_selftest(int64_t limit_ns, moe_stream_t stream) {
 int moe_route_deepseek(const void* logits, moe_dtype_t dtype, int64_t rows, int32_t E,
                        const float* bias, const moe_route_params_t* params, int32_t* inds,
                        float* scores, moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(bias && (rows == 0 || (logits && inds && scores)), "NULL pointer argument");
     MOE_CHECK(dtype == MOE_DTYPE_F32 || dtype == MOE_DTYPE_BF16, "dtype %d unknown", (int)dtype);
     MOE_CHECK(rows >= 0, "rows = %lld < 0", (long long)rows);
@@ -502,13 +553,13 @@ int moe_route_deepseek(const void* logits, moe_dtype_t dtype, int64_t rows, int3
     a.inds = inds;
     a.scores = scores;
     a.logits_out = nullptr;
-    MOE_CUDA(moe::launch_route(a, (cudaStream_t)stream), "route kernel");
+    MOE_LAUNCH(moe::launch_route(a, (cudaStream_t)stream), "route kernel");
     return MOE_OK;
 }
 
 int moe_permute(const int32_t* inds, int64_t T, int32_t K, int32_t E, int32_t* counts,
                 int32_t* offsets, int32_t* perm, int32_t* inv_perm, moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(counts && offsets && (T * (int64_t)K == 0 || (inds && perm && inv_perm)),
               "NULL pointer argument");
     MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
@@ -517,7 +568,7 @@ int moe_permute(const int32_t* inds, int64_t T, int32_t K, int32_t E, int32_t* c
     MOE_CHECK(T * (int64_t)K < ((int64_t)1 << 31), "T*K too large");
     int rc = check_device();
     if (rc) return rc;
-    MOE_CUDA(moe::launch_permute(inds, T * K, E, counts, offsets, perm, inv_perm,
+    MOE_LAUNCH(moe::launch_permute(inds, T * K, E, counts, offsets, perm, inv_perm,
                                  (cudaStream_t)stream),
              "permute kernel");
     return MOE_OK;
@@ -525,7 +576,7 @@ int moe_permute(const int32_t* inds, int64_t T, int32_t K, int32_t E, int32_t* c
 
 int moe_router_logits(const void* x, int64_t T, int32_t d, const void* w_router, int32_t E,
                       const float* logit_offset, float* logits, moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(w_router && (T == 0 || (x && logits)), "NULL pointer argument");
     MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
     MOE_CHECK(d >= 64 && d % 64 == 0, "d = %d must be a positive multiple of 64", d);
@@ -553,9 +604,9 @@ int moe_router_logits(const void* x, int64_t T, int32_t d, const void* w_router,
     g.tok_tile = T <= 256 ? (T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128) : 0;
     const int tokn = g.tok_tile ? g.tok_tile : 128;
     g.max_tiles = ((T + tokn - 1) / tokn) * ((E + (g.tok_tile ? 127 : 255)) / (g.tok_tile ? 128 : 256));
-    MOE_CUDA(moe::launch_gemm(g, (cudaStream_t)stream), "router GEMM");
+    MOE_LAUNCH(moe::launch_gemm(g, (cudaStream_t)stream), "router GEMM");
     if (logit_offset)
-        MOE_CUDA(moe::launch_add_offset(logits, T, E, logit_offset, (cudaStream_t)stream),
+        MOE_LAUNCH(moe::launch_add_offset(logits, T, E, logit_offset, (cudaStream_t)stream),
                  "logit offset");
     return MOE_OK;
 }
@@ -571,7 +622,7 @@ int moe_grouped_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E
                        const int32_t* offsets, const int32_t* perm,
                        const moe_expert_weights_t* experts, const moe_expert_weights_t* shared,
                        void* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(offsets && ws && (T == 0 || (x && perm && out)), "NULL pointer argument");
     int rc = check_dims(T, d, I, E, K);
     if (rc) return rc;
@@ -595,7 +646,7 @@ int moe_grouped_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E
 int moe_combine(const void* expert_out, const float* scores, const int32_t* inv_perm,
                 const void* shared_out, int64_t T, int32_t K, int32_t d, void* y,
                 moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(T == 0 || (expert_out && scores && inv_perm && y), "NULL pointer argument");
     MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
     MOE_CHECK(K >= 1, "K = %d < 1", K);
@@ -605,7 +656,7 @@ int moe_combine(const void* expert_out, const float* scores, const int32_t* inv_
     if (T == 0) return MOE_OK;
     int rc = check_device();
     if (rc) return rc;
-    MOE_CUDA(moe::launch_combine(expert_out, scores, inv_perm, shared_out, T, K, d, y,
+    MOE_LAUNCH(moe::launch_combine(expert_out, scores, inv_perm, shared_out, T, K, d, y,
                                  (cudaStream_t)stream),
              "combine kernel");
     return MOE_OK;
@@ -623,7 +674,7 @@ int moe_forward(const void* x, int64_t T, int32_t d, int32_t I, int32_t E,
                 const moe_expert_weights_t* shared, void* y, int32_t* inds_out,
                 float* scores_out, float* logits_out, void* ws, size_t ws_bytes,
                 moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(params, "params is NULL");
     moe_layer_args_t a = {};
     a.route_kind = MOE_ROUTE_DEEPSEEK;
@@ -652,14 +703,14 @@ size_t moe_forward_ex_workspace_bytes(const moe_layer_args_t* a) {
 }
 
 int moe_forward_ex(const moe_layer_args_t* args, void* ws, size_t ws_bytes, moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(args, "args is NULL");
     return forward_impl(*args, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 int moe_route_softmax(const void* logits, moe_dtype_t dtype, int64_t rows, int32_t E,
                       int32_t top_k, int32_t* inds, float* scores, moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(rows == 0 || (logits && inds && scores), "NULL pointer argument");
     MOE_CHECK(dtype == MOE_DTYPE_F32 || dtype == MOE_DTYPE_BF16, "dtype %d unknown", (int)dtype);
     MOE_CHECK(rows >= 0, "rows = %lld < 0", (long long)rows);
@@ -682,13 +733,13 @@ int moe_route_softmax(const void* logits, moe_dtype_t dtype, int64_t rows, int32
     a.inds = inds;
     a.scores = scores;
     a.softmax = 1;
-    MOE_CUDA(moe::launch_route(a, (cudaStream_t)stream), "route kernel");
+    MOE_LAUNCH(moe::launch_route(a, (cudaStream_t)stream), "route kernel");
     return MOE_OK;
 }
 
 int moe_shared_gate(const void* x, int64_t T, int32_t d, const void* w_gate, float* gate,
                     moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(w_gate && (T == 0 || (x && gate)), "NULL pointer argument");
     MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
     MOE_CHECK(d >= 8 && d % 8 == 0, "d = %d must be a positive multiple of 8", d);
@@ -696,14 +747,14 @@ int moe_shared_gate(const void* x, int64_t T, int32_t d, const void* w_gate, flo
     if (T == 0) return MOE_OK;
     int rc = check_device();
     if (rc) return rc;
-    MOE_CUDA(moe::launch_shared_gate(x, T, d, w_gate, gate, (cudaStream_t)stream), "shared gate");
+    MOE_LAUNCH(moe::launch_shared_gate(x, T, d, w_gate, gate, (cudaStream_t)stream), "shared gate");
     return MOE_OK;
 }
 
 int moe_combine_gated(const void* expert_out, const float* scores, const int32_t* inv_perm,
                       const void* shared_out, const float* shared_gate, int64_t T, int32_t K,
                       int32_t d, void* y, moe_stream_t stream) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(T == 0 || (expert_out && scores && inv_perm && shared_out && shared_gate && y),
               "NULL pointer argument");
     MOE_CHECK(T >= 0, "T = %lld < 0", (long long)T);
@@ -714,14 +765,33 @@ int moe_combine_gated(const void* expert_out, const float* scores, const int32_t
     if (T == 0) return MOE_OK;
     int rc = check_device();
     if (rc) return rc;
-    MOE_CUDA(moe::launch_combine(expert_out, scores, inv_perm, shared_out, T, K, d, y,
+    MOE_LAUNCH(moe::launch_combine(expert_out, scores, inv_perm, shared_out, T, K, d, y,
                                  (cudaStream_t)stream, shared_gate),
              "combine kernel");
     return MOE_OK;
 }
 
+int moe_set_fault(int32_t kind, int32_t at) {
+    begin_call();
+    MOE_CHECK(kind == MOE_FAULT_NONE || kind == MOE_FAULT_LAUNCH, "fault kind %d unknown", kind);
+    MOE_CHECK(at >= 0, "at = %d < 0", at);
+    fault_init();
+    g_fault_at.store(at, std::memory_order_relaxed);
+    g_fault_kind.store(kind, std::memory_order_release);
+    return MOE_OK;
+}
+
+int moe_get_fault(int32_t* kind, int32_t* at) {
+    begin_call();
+    MOE_CHECK(kind && at, "NULL pointer argument");
+    fault_init();
+    *kind = g_fault_kind.load(std::memory_order_acquire);
+    *at = g_fault_at.load(std::memory_order_relaxed);
+    return MOE_OK;
+}
+
 int moe_set_phase_events(void* const* events, int32_t n) {
-    g_err.clear();
+    begin_call();
     MOE_CHECK(n >= 0 && n <= kMaxPhaseEvents, "n = %d outside [0, %d]", n, kMaxPhaseEvents);
     MOE_CHECK(n == 0 || events, "events is NULL");
     for (int i = 0; i < n; ++i) g_phase_ev[i] = static_cast<cudaEvent_t>(events[i]);

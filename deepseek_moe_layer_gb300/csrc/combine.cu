@@ -8,8 +8,9 @@
 // With the gated shared expert (the combine's has_shared_expert_gate) the shared row is
 // weighted by a per-token sigmoid gate instead of 1.
 //
-// Grid (d / (8 * 128), T): each thread owns 8 consecutive features of one token and reads
-// K + 1 16-byte vectors, so the kernel streams the expert rows once at full width.
+// Grid (d / (8 * 128), min(T, 65535)): each thread owns 8 consecutive features of a token
+// and reads K + 1 16-byte vectors, so the kernel streams the expert rows once at full width;
+// the blocks of one grid row stride over the tokens (grid.y is capped at 65535).
 #include "common.cuh"
 #include "launch.h"
 
@@ -22,54 +23,55 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
                                                       const uint4* __restrict__ so,
                                                       const float* __restrict__ sgate, long long T,
                                                       int K, int vec_per_row, uint4* __restrict__ y) {
-    const long long t = blockIdx.y;
     const int v = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= T || v >= vec_per_row) return;
-    float acc[8];
+    if (v >= vec_per_row) return;
+    for (long long t = blockIdx.y; t < T; t += gridDim.y) {
+        float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    // K rows in chunks of 4: the chunk's slot ids, then its rows, all in flight together;
-    // the sum still runs k = 0, 1, .., K-1
-    for (int k0 = 0; k0 < K; k0 += 4) {
-        int jj[4];
-        float ww[4];
-        uint4 qq[4];
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        // K rows in chunks of 4: the chunk's slot ids, then its rows, all in flight together;
+        // the sum still runs k = 0, 1, .., K-1
+        for (int k0 = 0; k0 < K; k0 += 4) {
+            int jj[4];
+            float ww[4];
+            uint4 qq[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            jj[c] = k0 + c < K ? __ldg(inv + t * K + k0 + c) : -1;
-            ww[c] = k0 + c < K ? __ldg(scores + t * K + k0 + c) : 0.0f;
-        }
+            for (int c = 0; c < 4; ++c) {
+                jj[c] = k0 + c < K ? __ldg(inv + t * K + k0 + c) : -1;
+                ww[c] = k0 + c < K ? __ldg(scores + t * K + k0 + c) : 0.0f;
+            }
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            qq[c] = jj[c] >= 0 ? __ldg(eo + (long long)jj[c] * vec_per_row + v)
-                               : make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < 4; ++c)
+                qq[c] = jj[c] >= 0 ? __ldg(eo + (long long)jj[c] * vec_per_row + v)
+                                   : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            if (jj[c] < 0) continue;
-            const uint32_t u[4] = {qq[c].x, qq[c].y, qq[c].z, qq[c].w};
+            for (int c = 0; c < 4; ++c) {
+                if (jj[c] < 0) continue;
+                const uint32_t u[4] = {qq[c].x, qq[c].y, qq[c].z, qq[c].w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = fmaf(ww[c], bf16_lo(u[i]), acc[2 * i]);
-                acc[2 * i + 1] = fmaf(ww[c], bf16_hi(u[i]), acc[2 * i + 1]);
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = fmaf(ww[c], bf16_lo(u[i]), acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(ww[c], bf16_hi(u[i]), acc[2 * i + 1]);
+                }
             }
         }
-    }
-    if (so) {
-        const uint4 q = __ldg(so + t * vec_per_row + v);
-        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-        const float gw = sgate ? sgate[t] : 1.0f;  // gated shared expert: sigmoid weight
+        if (so) {
+            const uint4 q = __ldg(so + t * vec_per_row + v);
+            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+            const float gw = sgate ? sgate[t] : 1.0f;  // gated shared expert: sigmoid weight
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc[2 * i] = fmaf(gw, bf16_lo(u[i]), acc[2 * i]);
-            acc[2 * i + 1] = fmaf(gw, bf16_hi(u[i]), acc[2 * i + 1]);
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] = fmaf(gw, bf16_lo(u[i]), acc[2 * i]);
+                acc[2 * i + 1] = fmaf(gw, bf16_hi(u[i]), acc[2 * i + 1]);
+            }
         }
+        uint4 r;
+        r.x = pack_bf16x2(acc[0], acc[1]);
+        r.y = pack_bf16x2(acc[2], acc[3]);
+        r.z = pack_bf16x2(acc[4], acc[5]);
+        r.w = pack_bf16x2(acc[6], acc[7]);
+        y[t * vec_per_row + v] = r;
     }
-    uint4 r;
-    r.x = pack_bf16x2(acc[0], acc[1]);
-    r.y = pack_bf16x2(acc[2], acc[3]);
-    r.z = pack_bf16x2(acc[4], acc[5]);
-    r.w = pack_bf16x2(acc[6], acc[7]);
-    y[t * vec_per_row + v] = r;
 }
 
 // gate[t] = sigmoid(x[t] . w): one warp per token, 16-byte loads, fp32 products summed by
@@ -111,7 +113,7 @@ cudaError_t launch_combine(const void* expert_out, const float* scores, const in
                            cudaStream_t s, const float* shared_gate) {
     if (T == 0) return cudaSuccess;
     const int vpr = d / 8;
-    dim3 grid((unsigned)((vpr + 127) / 128), (unsigned)T);
+    dim3 grid((unsigned)((vpr + 127) / 128), (unsigned)(T < 65535 ? T : 65535));
     combine_kernel<<<grid, 128, 0, s>>>(static_cast<const uint4*>(expert_out), scores, inv,
                                         static_cast<const uint4*>(shared_out), shared_gate, T, K,
                                         vpr,

@@ -993,12 +993,10 @@ template <int MODE, int TOKT, int QB, int QG>
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
     using C = Cfg<MODE, TOKT, QB>;
     constexpr bool Q4 = C::kQ;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, TOKT, QB, QG>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        C::kSmemBytes);
+    static DeviceOnce attr_once;
+    const cudaError_t attr_err = attr_once.run([] {
+        return cudaFuncSetAttribute(moe_gemm_kernel<MODE, TOKT, QB, QG>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
 

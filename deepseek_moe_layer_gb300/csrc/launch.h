@@ -7,7 +7,36 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace moe {
+
+// One-time set-up that CUDA keeps per device (a kernel's dynamic shared-memory limit, for
+// instance): run() calls fn() the first time it is reached with a given device current and
+// remembers a success; a failure is returned and retried on the next call.  Safe to call
+// from several host threads.
+class DeviceOnce {
+  public:
+    static constexpr int kMaxDevices = 64;
+    template <class F>
+    cudaError_t run(F&& fn) {
+        int dev = -1;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+        e = fn();
+        if (e == cudaSuccess) done_[dev].store(1, std::memory_order_release);
+        return e;
+    }
+
+  private:
+    std::mutex mu_;
+    std::atomic<int> done_[kMaxDevices] = {};
+};
 
 // ---- gate ---------------------------------------------------------------------------
 struct RouteArgs {

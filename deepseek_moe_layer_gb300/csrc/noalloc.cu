@@ -2,11 +2,10 @@
 //
 // Some callers of this layer have no way to obtain a workspace: a serving engine that
 // reserves nearly all of HBM up front for its own pools (KV cache, weights) and hands out
-// nothing else, code running inside CUDA stream capture (where cudaMalloc is not allowed),
-// or a host program embedded in a framework that owns the allocator.  For them the
-// workspace of the whole layer lives in a fixed array in this library's own device memory,
-// sized for decode batches (about 169 tokens at DeepSeek-V3 shape).  The caller still
-// passes its inputs, weights and outputs.
+// nothing else, or a host program embedded in a framework that owns the allocator.  For
+// them the workspace of the whole layer lives in a fixed array in this library's own device
+// memory, sized for decode batches (up to 227 tokens at DeepSeek-V3 shape).  The caller
+// still passes its inputs, weights and outputs.
 //
 // Behaviour a caller must know:
 //   - The array is MOE_NOALLOC_SCRATCH_BYTES (64 MiB) on every device that loads the

@@ -282,17 +282,17 @@ cudaError_t launch_permute(const int32_t* inds, long long P, int E, int32_t* cou
                            int32_t* offsets, int32_t* perm, int32_t* inv, cudaStream_t s,
                            void* scratch, size_t scratch_bytes) {
     const size_t smem = sizeof(int32_t) * ((size_t)kPermWarps * E + 32);
-    static bool attr_done = false;
-    if (!attr_done) {
+    static DeviceOnce attr_once;
+    const cudaError_t attr_err = attr_once.run([] {
         const int most = (int)(sizeof(int32_t) * (kPermWarps * 1024 + 32));
         cudaError_t err = cudaFuncSetAttribute(permute_kernel,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, most);
         if (err == cudaSuccess)
             err = cudaFuncSetAttribute(permute_place_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-        if (err != cudaSuccess) return err;
-        attr_done = true;
-    }
+        return err;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
     if (P >= kPermMultiMin && scratch && scratch_bytes >= permute_scratch_bytes(E)) {
         const long long chunk = (P + kPermCtas - 1) / kPermCtas;
         int32_t* cnt = static_cast<int32_t*>(scratch);

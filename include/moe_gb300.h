@@ -297,12 +297,12 @@ size_t moe_forward_ex_workspace_bytes(const moe_layer_args_t* args);
 /*
  * moe_forward_noalloc -- moe_forward without a caller workspace.  The pages have no
  * counterpart: it exists for callers that cannot allocate device memory — serving engines
- * that reserve nearly all of HBM for their own pools, code running under CUDA stream
- * capture (where cudaMalloc is not allowed), hosts whose allocator belongs to another
- * framework.  Arguments and results are those of moe_forward minus ws / ws_bytes.
+ * that reserve nearly all of HBM for their own pools up front and hand out nothing else,
+ * hosts whose device allocator belongs to another framework.  Arguments and results are
+ * those of moe_forward minus ws / ws_bytes.
  *   - The workspace is a fixed array of MOE_NOALLOC_SCRATCH_BYTES (64 MiB) in the
  *     library's own device memory, held on every device that loads the library until the
- *     process exits; it fits decode batches (up to about 169 tokens at d = 7168, E = 256,
+ *     process exits; it fits decode batches (up to 227 tokens at d = 7168, E = 256,
  *     I = 2048, top_k = 8 with a shared expert).  A layer whose
  *     moe_forward_workspace_bytes() exceeds it is rejected with MOE_ERR_INVALID before
  *     anything runs.
@@ -319,6 +319,26 @@ int moe_forward_noalloc(const void* x, int64_t T, int32_t d, int32_t I, int32_t 
                         const moe_route_params_t* params, const moe_expert_weights_t* experts,
                         const moe_expert_weights_t* shared, void* y, int32_t* inds_out,
                         float* scores_out, float* logits_out, moe_stream_t stream);
+
+/*
+ * moe_set_fault / moe_get_fault -- host-side fault injection, a test hook with no
+ * counterpart in the pages (which fix only the contract it exercises: outputs unchanged on
+ * a rejected call).  With kind MOE_FAULT_LAUNCH the at-th kernel launch (0-based) of every
+ * following API call is not made: the call returns MOE_ERR_CUDA at that point, with
+ * moe_last_error() naming the step and "injected launch fault".  Kernels launched before it
+ * in the same call have run and written what they write; nothing after it runs.  In
+ * moe_forward the launches are, in order: 0 router linear, 1 gate, 2 dispatch, 3 token
+ * gather, 4 gate/up GEMM, 5 down GEMM, then (moe_forward_ex with a shared-expert gate) the
+ * shared gate, then the combine, the only launch that writes y.  The gate is the first
+ * launch that writes inds_out / scores_out / logits_out.  The count restarts at every entry
+ * point and is kept per host thread.  MOE_FAULT_NONE turns the hook off.
+ * The environment variable MOE_FAULT=launch or MOE_FAULT=launch:N sets the initial state
+ * (read once, at the first call that needs it).
+ * Errors: MOE_ERR_INVALID for an unknown kind, at < 0, NULL pointers.  Process-wide setting.
+ */
+enum { MOE_FAULT_NONE = 0, MOE_FAULT_LAUNCH = 1 };
+int moe_set_fault(int32_t kind, int32_t at);
+int moe_get_fault(int32_t* kind, int32_t* at);
 
 /*
  * moe_set_phase_events -- a timing aid with no counterpart in the pages: while set,

@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 import subprocess
+import sys
 
 import pytest
 import torch
@@ -196,3 +197,53 @@ def test_softmax_gate_watchdog_validation():
     for bad in (0, 999, 2_000_000_000):
         assert L.moe_watchdog_selftest(bad, None) == binding.MOE_ERR_INVALID
         assert "limit_ns" in L.moe_last_error().decode()
+
+
+def _align256(v):
+    return (v + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("T,d,I,E,K", [(128, 7168, 2048, 256, 8), (8192, 7168, 2048, 256, 8),
+                                       (64, 256, 128, 16, 4), (33, 640, 128, 24, 6)])
+def test_forward_workspace_layout_and_router_split_bound(T, d, I, E, K):
+    """The workspace is the documented pieces, with room for the router's partial logits of
+    at most max(1, d/512) K-splits: the router keeps at least 8 of its d/64 k-blocks per
+    split, so no device's plan splits further."""
+    P = T * K
+    S = max(1, d // 512)
+    want = (_align256(S * T * E * 4) + 2 * _align256(P * 4) + _align256(E * 4)
+            + _align256((E + 1) * 4) + 2 * _align256(P * 4) + _align256((P + T) * d * 2)
+            + _align256(P * d * 2) + _align256((P + T) * I * 2))
+    assert binding.lib().moe_forward_workspace_bytes(T, d, I, E, K, 1) == want
+
+
+def test_fault_hook_state_and_validation():
+    L = binding.lib()
+    before = binding.get_fault()
+    try:
+        binding.set_fault(binding.MOE_FAULT_LAUNCH, 3)
+        assert binding.get_fault() == (binding.MOE_FAULT_LAUNCH, 3)
+        assert L.moe_set_fault(7, 0) == binding.MOE_ERR_INVALID
+        assert "fault kind 7" in L.moe_last_error().decode()
+        assert L.moe_set_fault(binding.MOE_FAULT_LAUNCH, -1) == binding.MOE_ERR_INVALID
+        assert binding.get_fault() == (binding.MOE_FAULT_LAUNCH, 3)  # rejected: unchanged
+        assert L.moe_get_fault(None, None) == binding.MOE_ERR_INVALID
+        # argument checks still come first: a bad call is rejected as invalid, not faulted
+        binding.set_fault(binding.MOE_FAULT_LAUNCH, 0)
+        rc, err = _route(top_k=0)
+        assert rc == binding.MOE_ERR_INVALID and "top_k" in err
+        if not torch.cuda.is_available():  # and so is the device check, before any launch
+            rc, err = _route()
+            assert rc == binding.MOE_ERR_NODEVICE
+    finally:
+        binding.set_fault(*before)
+
+
+@pytest.mark.parametrize("env,want", [("launch", (1, 0)), ("launch:5", (1, 5)),
+                                      ("bogus", (0, 0)), ("", (0, 0))])
+def test_fault_hook_reads_environment(env, want):
+    code = ("import sys; sys.path.insert(0, %r); from deepseek_moe_layer_gb300 import binding; "
+            "print(*binding.get_fault())" % os.path.dirname(os.path.dirname(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                       env={**os.environ, "MOE_FAULT": env}, check=True)
+    assert tuple(int(v) for v in r.stdout.split()) == want

@@ -1,6 +1,6 @@
 """moe_forward_noalloc: the layer for callers that cannot allocate device memory (engines
-that reserve all of HBM for their own pools, code under CUDA stream capture, hosts whose
-allocator belongs to another framework).  Its workspace is a fixed 64 MiB array inside the
+that reserve all of HBM for their own pools, hosts whose device allocator belongs to another
+framework).  Its workspace is a fixed 64 MiB array inside the
 library, so these tests call it through the C ABI and hold it to the same results as
 moe_forward with a caller workspace, on two calls in a row (the second call finds the
 first call's data in the shared array and must not depend on it)."""
