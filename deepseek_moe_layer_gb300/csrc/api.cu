@@ -189,6 +189,16 @@ int expert_tok_tile(int64_t P, int32_t E, int32_t bits) {
     return 0;
 }
 
+// bf16 expert GEMMs with tokens on M run as CTA pairs (256-row tiles, cta_group::2 UMMAs)
+// when the experts see many tokens: a pair streams a third fewer operand bytes per unit of
+// tensor work and keeps six stages in flight instead of four (measured with 32 experts at
+// 8192 tokens: gate/up 2.90 -> 2.76 ms, down 1.47 -> 1.41 ms), but an expert's last tile is
+// padded to 256 rows instead of 128, and an UMMA costs the same whatever the share of real
+// rows (with 256 experts at 8192 tokens, ~590 rows per expert hit: 3.27 -> 3.43 ms).
+int expert_pair_tiles(int64_t P, int32_t E, int tok_tile, int32_t bits) {
+    return tok_tile == 0 && bits == 16 && P >= (int64_t)1024 * E ? 1 : 0;
+}
+
 struct RouterPlan {
     int tok_tile;
     int ksplit;
@@ -295,6 +305,7 @@ int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_
     g.out = h;
     g.out_ld = I;
     g.tok_tile = tok;
+    g.pair = expert_pair_tiles(P, E, tok, ex->bits);
     g.max_tiles = mt_bound * (I / 128);
     MOE_LAUNCH(moe::launch_gemm(g, s), "gate/up GEMM");
     MOE_CUDA(phase(5, s), "phase event");
@@ -320,6 +331,7 @@ int run_swiglu(const void* x, int64_t T, int32_t d, int32_t I, int32_t E, int32_
     const long long mt_dn = tok_dn == tok ? mt_bound
                                           : (P + 127) / 128 + E + (has_shared ? (T + 127) / 128 : 0);
     dn.tok_tile = tok_dn;
+    dn.pair = expert_pair_tiles(P, E, tok_dn, ex->bits);
     dn.max_tiles = mt_dn * ((d + (tok_dn ? 127 : 255)) / (tok_dn ? 128 : 256));
     MOE_LAUNCH(moe::launch_gemm(dn, s), "down GEMM");
     MOE_CUDA(phase(6, s), "phase event");
@@ -479,6 +491,9 @@ int moe_device_status(int32_t clear, moe_stream_t stream) {
     if (rc) return rc;
     unsigned int st = 0;
     MOE_CUDA(moe::read_device_status(&st, clear, (cudaStream_t)stream), "status read");
+    if (st == 5)
+        return fail(MOE_ERR_CUDA, "a CTA pair of an expert GEMM held different TMEM columns "
+                                  "(status %u); the GEMM did no work", st);
     if (st != 0) return fail(MOE_ERR_TIMEOUT, "a device-side wait gave up (status %u)", st);
     return MOE_OK;
 }

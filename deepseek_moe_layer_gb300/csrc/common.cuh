@@ -14,6 +14,7 @@ namespace moe {
 
 // Status codes written to the per-device status word (mirrors the public header).
 constexpr unsigned int kStatusTimeout = 3u;
+constexpr unsigned int kStatusPairTmem = 5u;  // the two CTAs of a pair hold different TMEM
 
 // A device-side wait gives up after this long (nanoseconds of %globaltimer).  The
 // longest legitimate wait is one tile's main loop, well under a millisecond.
@@ -90,6 +91,59 @@ MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
 }
 
 // ------------------------------------------------------------------------------------
+// thread-block clusters (CTA pairs of the 2-CTA UMMA)
+// ------------------------------------------------------------------------------------
+MOE_DEV uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster; orders memory (release / acquire) at cluster scope.
+MOE_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+MOE_DEV uint32_t mapa_shared(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+MOE_DEV uint32_t ld_shared_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+// Arrive (release, cluster scope) on the mbarrier at the same offset in CTA `rank`.
+MOE_DEV void mbar_arrive_cluster(uint64_t* bar, uint32_t rank) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                     mapa_shared(bar, rank))
+                 : "memory");
+}
+// try_wait with acquire at cluster scope (the phase may have been completed by arrivals
+// from the peer CTA), with a suspend-time hint.
+MOE_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+MOE_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
+                               unsigned long long limit_ns = kWaitLimitNs) {
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_cluster(bar, parity, 200000u)) return true;
+        if (abort && *abort) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
+    }
+}
+
+// ------------------------------------------------------------------------------------
 // TMA (tiled tensor copies global -> shared, completion counted on an mbarrier)
 // ------------------------------------------------------------------------------------
 MOE_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x, int32_t y,
@@ -98,6 +152,16 @@ MOE_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int32
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+// CTA pair: the copy lands in this CTA's shared memory and its bytes complete on the mbarrier
+// at `bar_cluster` (a shared::cluster address, here the leader CTA's barrier).
+MOE_DEV void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int32_t x,
+                              int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
         : "memory");
 }
 MOE_DEV uint64_t policy_evict_first() {
@@ -134,6 +198,42 @@ MOE_DEV void tc_fence_before() {
 }
 MOE_DEV void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// CTA pairs (cta_group::2): one warp of EACH CTA of the pair executes the allocation; both
+// receive the same column address, and the pair's UMMAs use those columns in both CTAs.
+MOE_DEV void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+MOE_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// Pair UMMA, issued by one thread of the even CTA: D (M = 256: rows 0-127 in this CTA's
+// TMEM, 128-255 in the peer's, all N columns in both) (+)= A * B^T, where A's rows 0-127 are
+// in this CTA's shared memory at the descriptor's address and rows 128-255 at the same
+// address in the peer, and B's rows (N) are split the same way, N/2 in each CTA.
+MOE_DEV void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrives once on the mbarrier at `bar`'s offset in every CTA of `cta_mask` when the pair
+// UMMAs issued so far by this thread have completed.
+MOE_DEV void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, one CTA.

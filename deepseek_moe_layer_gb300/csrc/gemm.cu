@@ -26,6 +26,12 @@
 //       experts see few tokens (decode): the weight stream is the whole cost, and putting
 //       the tokens on N wastes no tensor work or shared-memory bandwidth on padding.
 //
+// CTA pairs (bf16 experts, tokens on M, many tokens per expert): the two CTAs of a
+// cluster compute one 256 x 256 tile with cta_group::2 UMMAs issued by the even CTA.  Each
+// CTA loads its own 128 token rows and half of the tile's 256 weight rows; the odd CTA's
+// copies complete on the even CTA's stage barrier, the UMMAs' completion is multicast to both
+// CTAs' stage and accumulator barriers, and both epilogues report to the even CTA.
+//
 // Warp roles (192 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer: a ring of kStages (activation tile, weight tile) stages;
 //   warp 1      TMEM owner and UMMA issuer (one elected lane); accumulators double
@@ -58,10 +64,15 @@ __host__ __device__ constexpr int pow2ceil(int v) {
 
 constexpr int kDequantWarps = 8;  // 4-bit variant: warps turning packed codes into bf16
 
-template <int MODE, int TOKT, int QB>
+template <int MODE, int TOKT, int QB, int PAIR = 0>
 struct Cfg {
     static constexpr bool kQ = QB != 0;                              // affine-quantised weights
     static constexpr bool kSwap = TOKT != 0;
+    // CTA pair (bf16 experts, tokens on M): the two CTAs of a cluster compute one 256 x 256
+    // tile with cta_group::2 UMMAs (M = 256: 128 token rows per CTA; N = 256: each CTA loads
+    // half of the weight rows), so each CTA streams 32 KB of operands per k-block instead of
+    // 48 KB for the same tensor work, and six stages fit in shared memory instead of four.
+    static constexpr bool kPair = PAIR != 0;
     // quantised experts with tokens on M: a tile is two 128-row token sub-tiles that share
     // every dequantised weight stage (each B tile feeds two UMMAs, one accumulator per
     // sub-tile), which halves the dequantisation work per flop.  The two accumulators fill
@@ -70,9 +81,10 @@ struct Cfg {
     // accumulators than they gain: 5.72 -> 6.17 ms at T=8192, so they keep 128-row tiles.)
     static constexpr bool kM2 = kQ && !kSwap && MODE != kRouter;
     static constexpr int kSub = kM2 ? 2 : 1;                         // token sub-tiles
-    static constexpr int kTok = kSwap ? TOKT : 128 * kSub;           // tokens per tile
+    static constexpr int kTok = kSwap ? TOKT : 128 * kSub;           // token rows per CTA tile
+    static constexpr int kTileRows = kPair ? 2 * kTok : kTok;        // token rows per tile
     static constexpr int kNW = (kSwap && MODE == kGateUp) ? 2 : 1;   // A weight tiles (swap)
-    static constexpr int kWRows = kSwap ? 128 * kNW : 256;           // weight rows per stage
+    static constexpr int kWRows = kSwap ? 128 * kNW : (kPair ? 128 : 256);  // weight rows / stage
     static constexpr int kFeat = kSwap ? 128 : (MODE == kGateUp ? 128 : 256);
     static constexpr int kXBytes = kTok * 128;
     static constexpr int kWBytes = kWRows * 128;
@@ -103,7 +115,7 @@ struct Cfg {
     static constexpr int kThreadsCta = kQ ? kThreads + 32 + 32 * kDequantWarps : kThreads;
     static constexpr int kTmemCols = kTA ? 512 : pow2ceil(cmax(32, kAccBufs * kAccCols));
     static constexpr int kN = kSwap ? kTok : 256;
-    static constexpr uint32_t kIdesc = idesc_bf16(128, kN);
+    static constexpr uint32_t kIdesc = idesc_bf16(kPair ? 256 : 128, kN);
     static constexpr int kMaxGroups = 1025;
     // shared memory: operand stages | raw stages | barriers | misc | tile prefix | row offsets
     static constexpr int kRawOff = kStages * kStageBytes;
@@ -129,6 +141,7 @@ struct Cfg {
                   "TMEM budget of the TMEM-A path");
     static_assert(!kQ || kRawStages >= 2, "raw ring depth");
     static_assert(QB == 0 || QB == 4 || QB == 8, "code width");
+    static_assert(!kPair || (!kQ && !kSwap && MODE != kRouter), "CTA pairs: bf16, tokens on M");
 };
 
 struct KParams {
@@ -245,7 +258,7 @@ struct TileInfo {
 // Tiles of group g: ceil(rows_g / kTok) token tiles x feature tiles x k splits.
 template <class C>
 MOE_DEV int group_tiles(long long rows, int ftiles, int ksplit) {
-    return (int)((rows + C::kTok - 1) / C::kTok) * ftiles * ksplit;
+    return (int)((rows + C::kTileRows - 1) / C::kTileRows) * ftiles * ksplit;
 }
 
 template <class C>
@@ -255,9 +268,11 @@ MOE_DEV long long group_rows(const KParams& p, const int32_t* rowoff, int g) {
     return (long long)(rowoff[g + 1] - rowoff[g]);
 }
 
+// Tile t of the tile list.  For a CTA pair, `rank` picks this CTA's 128 token rows of the
+// pair's 256 (rows may then be 0: the peer's half of a short tile).
 template <class C>
 MOE_DEV TileInfo decode_tile(const KParams& p, const int32_t* prefix, const int32_t* rowoff,
-                             int ngroups, int t) {
+                             int ngroups, int t, int rank = 0) {
     // largest g with prefix[g] <= t (empty groups repeat the prefix and are skipped)
     int lo = 0, hi = ngroups - 1;
     while (lo < hi) {
@@ -268,15 +283,16 @@ MOE_DEV TileInfo decode_tile(const KParams& p, const int32_t* prefix, const int3
     ti.g = lo;
     ti.shared = p.offsets && lo == p.E;
     const long long rows = group_rows<C>(p, rowoff, lo);
-    const int mt = (int)((rows + C::kTok - 1) / C::kTok);
+    const int mt = (int)((rows + C::kTileRows - 1) / C::kTileRows);
     const int ft = (p.F + C::kFeat - 1) / C::kFeat;
     int local = t - prefix[lo];
     const int m = local % mt;
     local /= mt;
     ti.f = local % ft;
     ti.ks = local / ft;
-    const long long r0 = (long long)m * C::kTok;
-    ti.rows = (int)((rows - r0) < C::kTok ? (rows - r0) : C::kTok);
+    const long long r0 = (long long)m * C::kTileRows + (long long)rank * C::kTok;
+    const long long left = rows - r0;
+    ti.rows = (int)(left < 0 ? 0 : (left < C::kTok ? left : C::kTok));
     if (ti.shared) {
         ti.act_row = p.shared_act_row0 + r0;
         ti.out_row = p.shared_out_row0 + r0;
@@ -298,15 +314,15 @@ MOE_DEV void record_timeout(volatile int* abort) {
 
 // tm_w0 / tm_w1: bf16 weight rows (Q4 = false) or packed 4-bit code rows (Q4 = true); the
 // shared expert's maps tm_sw0 / tm_sw1 are always bf16.
-template <int MODE, int TOKT, int QB, int QG>
-__global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
+template <int MODE, int TOKT, int QB, int QG, int PAIR>
+__global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_act,
                     const __grid_constant__ CUtensorMap tm_act_sh,
                     const __grid_constant__ CUtensorMap tm_w0,
                     const __grid_constant__ CUtensorMap tm_w1,
                     const __grid_constant__ CUtensorMap tm_sw0,
                     const __grid_constant__ CUtensorMap tm_sw1, const KParams p) {
-    using C = Cfg<MODE, TOKT, QB>;
+    using C = Cfg<MODE, TOKT, QB, PAIR>;
     constexpr bool Q4 = C::kQ;  // any affine-quantised width (4 or 8 bits)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -327,10 +343,17 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ngroups = p.offsets ? p.E + p.has_shared : 1;
     const int ftiles = (p.F + C::kFeat - 1) / C::kFeat;
+    // CTA pair: rank 0 (the leader) issues the pair's UMMAs; both CTAs walk the same tiles
+    const int crank = C::kPair ? (int)cluster_rank() : 0;
+    const bool leader = crank == 0;
+    const int tstart = C::kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int tstep = C::kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     // ---- set-up: barriers, TMEM, group offsets and the tile prefix ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
+            // a pair's stage s completes on the leader's full[s]: the leader's arrival
+            // expects the bytes of both CTAs' copies
             mbar_init(&full[s], Q4 ? 1 + kDequantWarps : 1);
             mbar_init(&empty[s], 1);
         }
@@ -340,8 +363,9 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
         }
         mbar_init(&tfull[0], 1);
         mbar_init(&tfull[1], 1);
-        mbar_init(&tempty[0], 128);
-        mbar_init(&tempty[1], 128);
+        // pair: one arrival per epilogue warp of both CTAs (on the leader's barrier)
+        mbar_init(&tempty[0], C::kPair ? 8 : 128);
+        mbar_init(&tempty[1], C::kPair ? 8 : 128);
         mbar_init(done, 1);
         *abort = 0;
         fence_mbar_init();
@@ -352,7 +376,10 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
         prefetch_tmap(&tm_sw0);
         prefetch_tmap(&tm_sw1);
     }
-    if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+    if (warp == 1) {
+        if constexpr (C::kPair) tmem_alloc_pair(tmem_slot, C::kTmemCols);
+        else tmem_alloc(tmem_slot, C::kTmemCols);
+    }
     if (p.offsets)
         for (int i = threadIdx.x; i <= p.E; i += blockDim.x) rowoff[i] = p.offsets[i];
     __syncthreads();
@@ -378,7 +405,16 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = prefix[ngroups];
+    int total = prefix[ngroups];
+    if constexpr (C::kPair) {
+        // the peer's barriers are initialised and its TMEM allocated beyond this point; the
+        // pair's UMMAs address the same columns in both CTAs, so both must hold them
+        cluster_sync();
+        if (ld_shared_cluster_u32(mapa_shared(tmem_slot, (uint32_t)(crank ^ 1))) != tmem_base) {
+            total = 0;
+            if (threadIdx.x == 0) atomicCAS(&g_status, 0u, kStatusPairTmem);
+        }
+    }
 
     if (warp == 0) {
         // =============================== TMA producer ===============================
@@ -387,8 +423,8 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
             const uint64_t pol_x = policy_evict_last();
             int it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
+            for (int t = tstart; t < total && ok; t += tstep) {
+                const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t, crank);
                 const CUtensorMap* am = ti.shared ? &tm_act_sh : &tm_act;
                 const CUtensorMap* w0 = ti.shared ? &tm_sw0 : &tm_w0;
                 const CUtensorMap* w1 = ti.shared ? &tm_sw1 : &tm_w1;
@@ -407,6 +443,23 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                         tma_load_2d(st, am, &full[s], kx, (int)ti.act_row, pol_x);
                         continue;
                     }
+                    if (C::kPair) {
+                        // this CTA's token rows and its half of the pair's 256 weight rows
+                        // (gate rows in the leader, up rows in the peer, or the first /
+                        // second 128 down rows), both completing on the leader's full[s]
+                        const int wr = MODE == kGateUp ? wrow : wrow + crank * 128;
+                        const CUtensorMap* wm = (MODE == kGateUp && crank) ? w1 : w0;
+                        if (leader) {
+                            mbar_arrive_expect_tx(&full[s], 2 * (C::kXBytes + C::kWBytes));
+                            tma_load_2d(st, am, &full[s], kx, (int)ti.act_row, pol_x);
+                            tma_load_2d(wst, wm, &full[s], kx, wr, pol_w);
+                        } else {
+                            const uint32_t lb = mapa_shared(&full[s], 0);
+                            tma_load_2d_pair(st, am, lb, kx, (int)ti.act_row, pol_x);
+                            tma_load_2d_pair(wst, wm, lb, kx, wr, pol_w);
+                        }
+                        continue;
+                    }
                     mbar_arrive_expect_tx(&full[s], C::kXBytes + C::kWBytes);
                     tma_load_2d(st, am, &full[s], kx, (int)ti.act_row, pol_x);
                     if (MODE == kGateUp) {
@@ -417,9 +470,10 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                     }
                 }
             }
-            if (!ok) {
+            if (!ok && leader) {
                 // let the copies already issued land before the CTA can exit (full[s] also
-                // waits for the dequant warps in the 4-bit case: bounded, then give up)
+                // waits for the dequant warps in the 4-bit case, and for the peer's copies in
+                // a pair: bounded, then give up)
                 for (int n = (it > C::kStages ? it - C::kStages : 0); n < it; ++n)
                     mbar_wait(&full[n % C::kStages], (uint32_t)(n / C::kStages) & 1u, nullptr,
                               100000000ull);
@@ -433,8 +487,8 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
             const uint64_t pol_w = policy_evict_first();
             int rit = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
+            for (int t = tstart; t < total && ok; t += tstep) {
+                const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t, crank);
                 if (ti.shared) {
                     // normal-mode 4-bit: the operand producer loads the bf16 shared rows;
                     // TMEM-A path: one k-block of them per raw slot (same 128-byte rows)
@@ -475,22 +529,26 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                               nullptr, 100000000ull);
             }
         }
+    } else if (warp == 1 && C::kPair && !leader) {
+        // pair peer: the leader's thread issues the pair's UMMAs
     } else if (warp == 1) {
         // ================================ UMMA issuer ===============================
         if (lane == 0) {
             int it = 0, lt = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
-                const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
+            for (int t = tstart; t < total && ok; t += tstep, ++lt) {
+                const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t, crank);
                 const int ab = C::kAccBufs == 2 ? (lt & 1) : 0;
                 const uint32_t aph = (uint32_t)(C::kAccBufs == 2 ? (lt >> 1) : lt) & 1u;
-                if (!mbar_wait(&tempty[ab], aph ^ 1u, abort)) { record_timeout(abort); break; }
+                if (!(C::kPair ? mbar_wait_cluster(&tempty[ab], aph ^ 1u, abort)
+                               : mbar_wait(&tempty[ab], aph ^ 1u, abort))) { record_timeout(abort); break; }
                 tc_fence_after();
                 const uint32_t acc = tmem_base + (uint32_t)(ab * C::kAccCols);
                 for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++it) {
                     const int s = it % C::kStages;
                     const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
-                    if (!mbar_wait(&full[s], ph, abort)) { record_timeout(abort); ok = false; break; }
+                    if (!(C::kPair ? mbar_wait_cluster(&full[s], ph, abort)
+                                   : mbar_wait(&full[s], ph, abort))) { record_timeout(abort); ok = false; break; }
                     tc_fence_after();
                     const uint32_t xs = smem_u32(smem + s * C::kStageBytes);
                     const uint32_t ws = xs + C::kXBytes;
@@ -513,6 +571,9 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                                 umma_bf16(acc + (uint32_t)(w * C::kTok),
                                           sdesc_k128(ws + w * 128 * 128 + kk * 32), bd,
                                           C::kIdesc, accum);
+                        } else if (C::kPair) {
+                            umma_bf16_pair(acc, sdesc_k128(xs + kk * 32), sdesc_k128(ws + kk * 32),
+                                           C::kIdesc, accum);
                         } else {
                             const uint64_t bd = sdesc_k128(ws + kk * 32);
                             umma_bf16(acc, sdesc_k128(xs + kk * 32), bd, C::kIdesc, accum);
@@ -522,14 +583,17 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                                           C::kIdesc, accum);
                         }
                     }
-                    umma_commit(&empty[s]);
+                    if (C::kPair) umma_commit_pair(&empty[s], 3);  // both CTAs' stage s
+                    else umma_commit(&empty[s]);
                 }
                 if (!ok) break;
-                umma_commit(&tfull[ab]);
+                if (C::kPair) umma_commit_pair(&tfull[ab], 3);
+                else umma_commit(&tfull[ab]);
             }
             // drain every UMMA issued by this thread before TMEM can be released
             if (it > 0) {
-                umma_commit(done);
+                if (C::kPair) umma_commit_pair(done, 1);
+                else umma_commit(done);
                 mbar_wait(done, 0u, nullptr, 100000000ull);
             }
         }
@@ -567,8 +631,8 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
         };
         int it = 0, rit = 0;  // operand-ring and raw-ring positions
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
+        for (int t = tstart; t < total && ok; t += tstep) {
+            const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t, crank);
             const bool rvalid = !ti.shared && ti.f * C::kFeat + rr < p.F;
             const long long grow = (long long)ti.g * p.F + ti.f * C::kFeat + rr;
             const unsigned short* srow = sp + grow * ngr;
@@ -739,8 +803,8 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
         // ================================= epilogue =================================
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         int lt = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
-            const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t);
+        for (int t = tstart; t < total; t += tstep, ++lt) {
+            const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t, crank);
             const int ab = C::kAccBufs == 2 ? (lt & 1) : 0;
             const uint32_t aph = (uint32_t)(C::kAccBufs == 2 ? (lt >> 1) : lt) & 1u;
             if (!mbar_wait(&tfull[ab], aph, abort)) { record_timeout(abort); break; }
@@ -921,16 +985,29 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB>::kThreadsCta, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&tempty[ab]);
+            if constexpr (C::kPair) {
+                // one arrival per warp, on the leader's barrier (remote for the peer)
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader) mbar_arrive(&tempty[ab]);
+                    else mbar_arrive_cluster(&tempty[ab], 0);
+                }
+            } else {
+                mbar_arrive(&tempty[ab]);
+            }
         }
     }
 
     // ---- tear-down ----
     tc_fence_before();
     __syncthreads();
+    // a pair: neither CTA leaves while the other's UMMAs, copies or arrivals may still touch
+    // its shared memory or TMEM
+    if constexpr (C::kPair) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        if constexpr (C::kPair) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+        else tmem_dealloc(tmem_base, C::kTmemCols);
     }
 }
 
@@ -989,18 +1066,18 @@ bool make_map_q4(CUtensorMap* m, const void* base, long long rows, long long col
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int TOKT, int QB, int QG>
+template <int MODE, int TOKT, int QB, int QG, int PAIR = 0>
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
-    using C = Cfg<MODE, TOKT, QB>;
+    using C = Cfg<MODE, TOKT, QB, PAIR>;
     constexpr bool Q4 = C::kQ;
     static DeviceOnce attr_once;
     const cudaError_t attr_err = attr_once.run([] {
-        return cudaFuncSetAttribute(moe_gemm_kernel<MODE, TOKT, QB, QG>,
+        return cudaFuncSetAttribute(moe_gemm_kernel<MODE, TOKT, QB, QG, PAIR>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
 
-    const int wbox = C::kSwap ? 128 : (MODE == kGateUp ? 128 : 256);
+    const int wbox = C::kSwap ? 128 : (C::kPair || MODE == kGateUp ? 128 : 256);
     const long long wrows_routed = (long long)(a.offsets ? a.E : 1) * a.F;
     CUtensorMap m_act, m_act_sh, m_w0, m_w1, m_sw0, m_sw1;
     bool ok = make_map(&m_act, a.act, a.act_rows, a.Kdim, C::kTok);
@@ -1049,7 +1126,45 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
     long long grid = num_sms();
     if (a.max_tiles < grid) grid = a.max_tiles;
     if (grid < 1) return cudaSuccess;
-    moe_gemm_kernel<MODE, TOKT, QB, QG><<<(unsigned)grid, C::kThreadsCta, C::kSmemBytes, s>>>(
+    if constexpr (C::kPair) {
+        // persistent CTA pairs: clusters of two, one CTA per SM, as many pairs as the device
+        // can hold at once (an SM left over in a GPC of odd size takes no pair)
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(C::kThreadsCta, 1, 1);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        static int resident[DeviceOnce::kMaxDevices] = {};
+        static DeviceOnce occ_once;
+        int dev = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        if (dev < 0 || dev >= DeviceOnce::kMaxDevices) return cudaErrorInvalidDevice;
+        err = occ_once.run([&] {
+            cfg.gridDim = dim3((unsigned)(2 * (num_sms() / 2)), 1, 1);
+            int n = 0;
+            const cudaError_t e = cudaOccupancyMaxActiveClusters(
+                &n, moe_gemm_kernel<MODE, TOKT, QB, QG, PAIR>, &cfg);
+            if (e == cudaSuccess) resident[dev] = n > 0 ? n : 1;
+            return e;
+        });
+        if (err != cudaSuccess) return err;
+        long long pairs = resident[dev];
+        if (num_sms() / 2 < pairs) pairs = num_sms() / 2;
+        if (a.max_tiles < pairs) pairs = a.max_tiles;
+        if (pairs < 1) pairs = 1;
+        cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+        err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<MODE, TOKT, QB, QG, PAIR>,
+                                                   m_act, m_act_sh, m_w0, m_w1, m_sw0, m_sw1, p);
+        return err != cudaSuccess ? err : cudaGetLastError();
+    }
+    moe_gemm_kernel<MODE, TOKT, QB, QG, PAIR><<<(unsigned)grid, C::kThreadsCta, C::kSmemBytes, s>>>(
         m_act, m_act_sh, m_w0, m_w1, m_sw0, m_sw1, p);
     return cudaGetLastError();
 }
@@ -1060,7 +1175,10 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
 template <int MODE, int QB, int QG>
 cudaError_t dispatch_tok(const GemmArgs& a, cudaStream_t s) {
     switch (a.tok_tile) {
-        case 0: return run_gemm<MODE, 0, QB, QG>(a, s);
+        case 0:
+            if constexpr (QB == 0 && MODE != kRouter)
+                if (a.pair) return run_gemm<MODE, 0, QB, QG, 1>(a, s);
+            return run_gemm<MODE, 0, QB, QG>(a, s);
         case 16:
             if constexpr (MODE == kRouter) return run_gemm<MODE, 16, QB, QG>(a, s);
             return cudaErrorInvalidValue;

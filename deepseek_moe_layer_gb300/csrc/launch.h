@@ -137,6 +137,7 @@ struct GemmArgs {
     long long out_ld;
     int tok_tile;                // 0: tokens on the M side (128-row tiles); else tokens on
                                  // the N side in tiles of tok_tile (16/32/64/128)
+    int pair;                    // bf16, tokens on M: 256-row tiles on CTA pairs
     long long max_tiles;         // host upper bound on the number of tiles
 };
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);

@@ -130,6 +130,21 @@ def test_layer_multi_tile(T, d, I, E, K, G, tg):
     _check_forward(w, inputs.gen_layer(w, DEV, seed=1))
 
 
+# Experts averaging at least 1024 rows run their bf16 GEMMs on CTA pairs (256-row tiles,
+# cta_group::2 UMMAs): few experts, many tokens, ragged last tiles and several feature tiles.
+@pytest.mark.parametrize("T,d,I,E,K,G,tg,shared", [
+    (2048, 256, 128, 8, 4, 4, 2, True),      # 1024 rows per expert on average
+    (2600, 512, 384, 4, 2, 2, 1, True),      # d = 2 x 256 output tiles, I = 3 x 128
+    (3001, 640, 256, 6, 3, 3, 2, False),     # d not a multiple of 256, no shared expert
+])
+def test_layer_cta_pair_tiles(T, d, I, E, K, G, tg, shared):
+    w = inputs.Workload("pair", T=T, d=d, E=E, I=I, top_k=K, n_group=G, topk_group=tg,
+                        norm_topk_prob=True, routed_scaling_factor=2.5, bias_var=0.05,
+                        shared=shared)
+    assert T * K >= 1024 * E
+    _check_forward(w, inputs.gen_layer(w, DEV, seed=T), tile=128)
+
+
 def test_layer_without_shared_expert():
     w = inputs.scaled(inputs.WORKLOADS["tiny_T64_E16"], T=100, shared=False)
     _check_forward(w, inputs.gen_layer(w, DEV, seed=2))
