@@ -21,6 +21,15 @@
 namespace {
 
 thread_local std::string g_err;
+thread_local bool g_pdl = false;
+
+// Programmatic dependent launch for the rest of a layer call (restored on return).
+struct PdlScope {
+    bool prev;
+    PdlScope() : prev(g_pdl) {}
+    void on() { g_pdl = true; }
+    ~PdlScope() { g_pdl = prev; }
+};
 
 int fail(int code, const char* fmt, ...) {
     char buf[512];
@@ -427,6 +436,13 @@ int forward_impl(const moe_layer_args_t& A, void* ws, size_t ws_bytes, cudaStrea
     g.max_tiles = rp.tiles;
     MOE_LAUNCH(moe::launch_gemm(g, s), "router GEMM");
     MOE_CUDA(phase(1, s), "phase event");
+    // decode-sized batches: the layer's later kernels start while the one before them
+    // finishes (measured at T = 128: 1.099 -> 1.080 ms per layer).  Not for large batches
+    // (a programmatic launch of the prefill gate/up GEMM measured 5.49 -> 6.03 ms at T = 8192,
+    // where launch gaps are a negligible share anyway), nor while the phase events that time
+    // each kernel are recorded between them.
+    PdlScope pdl;
+    if (g_phase_n == 0 && T * K < moe::kPermMultiMin) pdl.on();
 
     // a2: gate (sums the partials in split order, adds the offset)
     moe::RouteArgs ra = {};
@@ -479,6 +495,8 @@ int moe::set_error(int code, const char* msg) {
     g_err = msg;
     return code;
 }
+
+bool moe::pdl_enabled() { return g_pdl; }
 
 extern "C" {
 

@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
                                                       const float* __restrict__ sgate, long long T,
                                                       int K, int vec_per_row, uint4* __restrict__ y) {
     const int v = blockIdx.x * blockDim.x + threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait();  // the expert outputs come from the kernels before
     if (v >= vec_per_row) return;
     for (long long t = blockIdx.y; t < T; t += gridDim.y) {
         float acc[8];
@@ -82,6 +84,8 @@ __global__ void __launch_bounds__(256) shared_gate_kernel(const uint4* __restric
                                                           float* __restrict__ gate) {
     const long long t = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait();  // writes nothing before the kernel before has finished
     if (t >= T) return;
     float acc = 0.0f;
     for (int v = lane; v < vec_per_row; v += 32) {
@@ -103,9 +107,8 @@ __global__ void __launch_bounds__(256) shared_gate_kernel(const uint4* __restric
 cudaError_t launch_shared_gate(const void* x, long long T, int d, const void* w, float* gate,
                                cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    shared_gate_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(
-        static_cast<const uint4*>(x), static_cast<const uint4*>(w), T, d / 8, gate);
-    return cudaGetLastError();
+    return launch_kernel(shared_gate_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, s,
+                         static_cast<const uint4*>(x), static_cast<const uint4*>(w), T, d / 8, gate);
 }
 
 cudaError_t launch_combine(const void* expert_out, const float* scores, const int32_t* inv,
@@ -114,11 +117,10 @@ cudaError_t launch_combine(const void* expert_out, const float* scores, const in
     if (T == 0) return cudaSuccess;
     const int vpr = d / 8;
     dim3 grid((unsigned)((vpr + 127) / 128), (unsigned)(T < 65535 ? T : 65535));
-    combine_kernel<<<grid, 128, 0, s>>>(static_cast<const uint4*>(expert_out), scores, inv,
-                                        static_cast<const uint4*>(shared_out), shared_gate, T, K,
-                                        vpr,
-                                        static_cast<uint4*>(y));
-    return cudaGetLastError();
+    return launch_kernel(combine_kernel, grid, dim3(128), 0, s,
+                         static_cast<const uint4*>(expert_out), scores, inv,
+                         static_cast<const uint4*>(shared_out), shared_gate, T, K, vpr,
+                         static_cast<uint4*>(y));
 }
 
 }  // namespace moe

@@ -91,6 +91,16 @@ MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
 }
 
 // ------------------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start while its predecessor in the stream still runs; it must not read the
+// predecessor's results nor write global memory before pdl_wait() (which returns at once
+// for a kernel launched the ordinary way).  pdl_launch_dependents() lets the next kernel
+// start launching as soon as every CTA of this one has issued it.
+// ------------------------------------------------------------------------------------
+MOE_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+MOE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ------------------------------------------------------------------------------------
 // thread-block clusters (CTA pairs of the 2-CTA UMMA)
 // ------------------------------------------------------------------------------------
 MOE_DEV uint32_t cluster_rank() {

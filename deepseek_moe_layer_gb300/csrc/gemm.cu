@@ -350,6 +350,9 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
     const int tstep = C::kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     // ---- set-up: barriers, TMEM, group offsets and the tile prefix ----
+    // (barriers, TMEM and the tensor maps touch nothing the kernel before writes: with a
+    // programmatic launch this overlaps that kernel's tail; pdl_wait() comes before the first
+    // read of its results)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             // a pair's stage s completes on the leader's full[s]: the leader's arrival
@@ -380,6 +383,7 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
         if constexpr (C::kPair) tmem_alloc_pair(tmem_slot, C::kTmemCols);
         else tmem_alloc(tmem_slot, C::kTmemCols);
     }
+    pdl_wait();
     if (p.offsets)
         for (int i = threadIdx.x; i <= p.E; i += blockDim.x) rowoff[i] = p.offsets[i];
     __syncthreads();
@@ -999,6 +1003,9 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
     }
 
     // ---- tear-down ----
+    // the next kernel may start launching now (not earlier: its blocks would sit resident
+    // through this kernel's whole main loop)
+    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     // a pair: neither CTA leaves while the other's UMMAs, copies or arrivals may still touch
@@ -1133,11 +1140,13 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
         cfg.blockDim = dim3(C::kThreadsCta, 1, 1);
         cfg.dynamicSmemBytes = C::kSmemBytes;
         cfg.stream = s;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         static int resident[DeviceOnce::kMaxDevices] = {};
@@ -1160,13 +1169,14 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
         if (a.max_tiles < pairs) pairs = a.max_tiles;
         if (pairs < 1) pairs = 1;
         cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+        cfg.numAttrs = pdl_enabled() ? 2 : 1;
         err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<MODE, TOKT, QB, QG, PAIR>,
                                                    m_act, m_act_sh, m_w0, m_w1, m_sw0, m_sw1, p);
         return err != cudaSuccess ? err : cudaGetLastError();
     }
-    moe_gemm_kernel<MODE, TOKT, QB, QG, PAIR><<<(unsigned)grid, C::kThreadsCta, C::kSmemBytes, s>>>(
-        m_act, m_act_sh, m_w0, m_w1, m_sw0, m_sw1, p);
-    return cudaGetLastError();
+    return launch_kernel(moe_gemm_kernel<MODE, TOKT, QB, QG, PAIR>, dim3((unsigned)grid),
+                         dim3(C::kThreadsCta), (size_t)C::kSmemBytes, s, m_act, m_act_sh, m_w0,
+                         m_w1, m_sw0, m_sw1, p);
 }
 
 // Token tiles: the router takes 16 / 32 / 64 / 128 tokens on N or 128 on M; the expert

@@ -152,4 +152,28 @@ int num_sms();
 // Sets the thread-local text returned by moe_last_error() and returns `code`.
 int set_error(int code, const char* msg);
 
+// Programmatic dependent launch for the kernels of one layer call after its first: while set
+// (per host thread), the launchers below launch with programmatic stream serialization, so a
+// kernel's prologue overlaps the tail of the one before it (each kernel waits with
+// griddepcontrol.wait before it reads its predecessor's results or writes global memory).
+bool pdl_enabled();
+
+// Launches `kernel` on `s`, with programmatic stream serialization when pdl_enabled().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return err != cudaSuccess ? err : cudaGetLastError();
+}
+
 }  // namespace moe

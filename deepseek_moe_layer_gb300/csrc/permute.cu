@@ -30,8 +30,10 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
     int32_t* hist = sh;                      // [kPermWarps][E]
     int32_t* wsum = sh + kPermWarps * E;     // [32] scan carries
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_launch_dependents();
 
     for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) hist[i] = 0;
+    pdl_wait();  // the expert ids come from the kernel before
     __syncthreads();
 
     const long long chunk = (P + kPermWarps - 1) / kPermWarps;
@@ -141,7 +143,9 @@ __global__ void __launch_bounds__(1024) permute_count_kernel(const int32_t* __re
                                                              long long P, int E, long long chunk,
                                                              int32_t* __restrict__ cnt) {
     extern __shared__ int32_t sh[];  // [E]
+    pdl_launch_dependents();
     for (int i = threadIdx.x; i < E; i += blockDim.x) sh[i] = 0;
+    pdl_wait();
     __syncthreads();
     const long long c0 = min(P, (long long)blockIdx.x * chunk);
     const long long c1 = min(P, c0 + chunk);
@@ -162,8 +166,10 @@ __global__ void __launch_bounds__(1024) permute_place_kernel(
     int32_t* wsum = sh + kPermWarps * E;     // [32] scan carries
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x, nb = gridDim.x;
+    pdl_launch_dependents();
 
     for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) hist[i] = 0;
+    pdl_wait();  // the per-chunk counts come from the kernel before
     // expert e (thread e, E <= 1024): its pairs in all chunks and in the chunks before b
     const int e_t = threadIdx.x;
     int tot = 0, pre = 0;
@@ -256,6 +262,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           uint4* __restrict__ x_perm) {
     const long long j = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait();  // the dispatch comes from the kernel before
     if (j >= P || j >= offsets[E]) return;
     const long long t = perm[j] / K;
     const uint4* src = x + t * vec_per_row;
@@ -296,23 +304,23 @@ cudaError_t launch_permute(const int32_t* inds, long long P, int E, int32_t* cou
     if (P >= kPermMultiMin && scratch && scratch_bytes >= permute_scratch_bytes(E)) {
         const long long chunk = (P + kPermCtas - 1) / kPermCtas;
         int32_t* cnt = static_cast<int32_t*>(scratch);
-        permute_count_kernel<<<kPermCtas, 1024, sizeof(int32_t) * (size_t)E, s>>>(inds, P, E,
-                                                                                   chunk, cnt);
-        permute_place_kernel<<<kPermCtas, 1024, smem, s>>>(inds, P, E, chunk, cnt, counts,
-                                                           offsets, perm, inv);
-        return cudaGetLastError();
+        cudaError_t err = launch_kernel(permute_count_kernel, dim3(kPermCtas), dim3(1024),
+                                        sizeof(int32_t) * (size_t)E, s, inds, P, E, chunk, cnt);
+        if (err != cudaSuccess) return err;
+        return launch_kernel(permute_place_kernel, dim3(kPermCtas), dim3(1024), smem, s, inds, P, E,
+                             chunk, (const int32_t*)cnt, counts, offsets, perm, inv);
     }
-    permute_kernel<<<1, 1024, smem, s>>>(inds, P, E, counts, offsets, perm, inv);
-    return cudaGetLastError();
+    return launch_kernel(permute_kernel, dim3(1), dim3(1024), smem, s, inds, P, E, counts, offsets,
+                         perm, inv);
 }
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t* offsets, int E,
                                int K, long long P, int d, void* x_perm, cudaStream_t s) {
     if (P == 0) return cudaSuccess;
     const unsigned grid = (unsigned)((P + 7) / 8);
-    gather_rows_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(x), perm, offsets, E, K, P,
-                                            d / 8, static_cast<uint4*>(x_perm));
-    return cudaGetLastError();
+    return launch_kernel(gather_rows_kernel, dim3(grid), dim3(256), 0, s,
+                         static_cast<const uint4*>(x), perm, offsets, E, K, P, d / 8,
+                         static_cast<uint4*>(x_perm));
 }
 
 }  // namespace moe

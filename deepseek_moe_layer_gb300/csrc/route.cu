@@ -74,6 +74,8 @@ MOE_DEV Top2 lane_top2(const uint32_t (&key)[EPL], const float (&val)[EPL], uint
 // Each warp handles rows warp_id, warp_id + nwarps, ... (grid sized to the SMs).
 template <int EPL, bool SOFTMAX>
 __global__ void __launch_bounds__(256, EPL <= 8 ? 4 : 1) route_kernel(const RouteArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // the logits come from the kernel before
     const int lane = threadIdx.x & 31;
     const long long nwarps = (long long)gridDim.x * 8;
     const int E = a.E;
@@ -369,22 +371,22 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     const unsigned grid = (unsigned)(want < cap ? want : cap);
     if (a.softmax) {
         switch (epl) {
-            case 1: route_kernel<1, true><<<grid, 256, 0, s>>>(a); break;
-            case 2: route_kernel<2, true><<<grid, 256, 0, s>>>(a); break;
-            case 4: route_kernel<4, true><<<grid, 256, 0, s>>>(a); break;
-            case 8: route_kernel<8, true><<<grid, 256, 0, s>>>(a); break;
-            case 16: route_kernel<16, true><<<grid, 256, 0, s>>>(a); break;
-            default: route_kernel<32, true><<<grid, 256, 0, s>>>(a); break;
+            case 1: return launch_kernel(route_kernel<1, true>, dim3(grid), dim3(256), 0, s, a);
+            case 2: return launch_kernel(route_kernel<2, true>, dim3(grid), dim3(256), 0, s, a);
+            case 4: return launch_kernel(route_kernel<4, true>, dim3(grid), dim3(256), 0, s, a);
+            case 8: return launch_kernel(route_kernel<8, true>, dim3(grid), dim3(256), 0, s, a);
+            case 16: return launch_kernel(route_kernel<16, true>, dim3(grid), dim3(256), 0, s, a);
+            default: return launch_kernel(route_kernel<32, true>, dim3(grid), dim3(256), 0, s, a);
         }
         return cudaGetLastError();
     }
     switch (epl) {
-        case 1: route_kernel<1, false><<<grid, 256, 0, s>>>(a); break;
-        case 2: route_kernel<2, false><<<grid, 256, 0, s>>>(a); break;
-        case 4: route_kernel<4, false><<<grid, 256, 0, s>>>(a); break;
-        case 8: route_kernel<8, false><<<grid, 256, 0, s>>>(a); break;
-        case 16: route_kernel<16, false><<<grid, 256, 0, s>>>(a); break;
-        default: route_kernel<32, false><<<grid, 256, 0, s>>>(a); break;
+        case 1: return launch_kernel(route_kernel<1, false>, dim3(grid), dim3(256), 0, s, a);
+        case 2: return launch_kernel(route_kernel<2, false>, dim3(grid), dim3(256), 0, s, a);
+        case 4: return launch_kernel(route_kernel<4, false>, dim3(grid), dim3(256), 0, s, a);
+        case 8: return launch_kernel(route_kernel<8, false>, dim3(grid), dim3(256), 0, s, a);
+        case 16: return launch_kernel(route_kernel<16, false>, dim3(grid), dim3(256), 0, s, a);
+        default: return launch_kernel(route_kernel<32, false>, dim3(grid), dim3(256), 0, s, a);
     }
     return cudaGetLastError();
 }
