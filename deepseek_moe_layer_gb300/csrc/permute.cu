@@ -254,13 +254,17 @@ __global__ void __launch_bounds__(1024) permute_place_kernel(
     }
 }
 
-// One warp per dispatched slot: x_perm[j] = x[perm[j] / K], 16-byte vectors.
+// x_perm[j] = x[perm[j] / K], 16-byte vectors.  Warp w takes piece w % pieces (128 vectors,
+// 2 KB) of slot w / pieces: four 16-byte loads in flight per lane, all before the stores, and
+// many warps per row, so that a small batch is not one warp's serial walk along a 14 KB row.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
                                                           const int32_t* __restrict__ perm,
                                                           const int32_t* __restrict__ offsets,
                                                           int E, int K, long long P, int vec_per_row,
-                                                          uint4* __restrict__ x_perm) {
-    const long long j = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+                                                          int pieces, uint4* __restrict__ x_perm) {
+    const long long wg = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const long long j = wg / pieces;
+    const int v0 = (int)(wg % pieces) * 128;
     const int lane = threadIdx.x & 31;
     pdl_launch_dependents();
     pdl_wait();  // the dispatch comes from the kernel before
@@ -268,18 +272,18 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     const long long t = perm[j] / K;
     const uint4* src = x + t * vec_per_row;
     uint4* dst = x_perm + j * vec_per_row;
-    // four 16-byte loads in flight per lane before the stores; the gathered rows are
-    // streamed out (evict-first) so that x, read K times, stays in L2
-    int v = lane;
-    for (; v + 96 < vec_per_row; v += 128) {
-        const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
-                    e = __ldg(src + v + 96);
-        __stcs(dst + v, a);
-        __stcs(dst + v + 32, b);
-        __stcs(dst + v + 64, c);
-        __stcs(dst + v + 96, e);
+    // the gathered rows are streamed out (evict-first) so that x, read K times, stays in L2
+    uint4 q[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int v = v0 + 32 * u + lane;
+        if (v < vec_per_row) q[u] = __ldg(src + v);
     }
-    for (; v < vec_per_row; v += 32) __stcs(dst + v, __ldg(src + v));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int v = v0 + 32 * u + lane;
+        if (v < vec_per_row) __stcs(dst + v, q[u]);
+    }
 }
 
 }  // namespace
@@ -317,9 +321,11 @@ cudaError_t launch_permute(const int32_t* inds, long long P, int E, int32_t* cou
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, const int32_t* offsets, int E,
                                int K, long long P, int d, void* x_perm, cudaStream_t s) {
     if (P == 0) return cudaSuccess;
-    const unsigned grid = (unsigned)((P + 7) / 8);
+    const int vpr = d / 8;
+    const int pieces = (vpr + 127) / 128;
+    const unsigned grid = (unsigned)((P * pieces + 7) / 8);
     return launch_kernel(gather_rows_kernel, dim3(grid), dim3(256), 0, s,
-                         static_cast<const uint4*>(x), perm, offsets, E, K, P, d / 8,
+                         static_cast<const uint4*>(x), perm, offsets, E, K, P, vpr, pieces,
                          static_cast<uint4*>(x_perm));
 }
 
