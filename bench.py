@@ -37,15 +37,12 @@ METRIC = "MoE-layer tokens/s (DSv3 shape, T=128 & T=8192); % of HBM/tensor roofl
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant kernel per
-# algorithmic byte, from an ncu capture of a reduced case of the same shapes (the full
-# workloads are too large to replay); traffic grows with the expert bytes processed, so the
-# per-launch traffic of the full workload is ratio x its algorithmic bytes.  Keyed by
-# workload with the hash of the GEMM sources the capture ran; a stale hash reports null.
+# algorithmic byte, from single-pass ncu captures of the full-size launches of these
+# workloads (routing is deterministic, so a launch's traffic is fixed), keyed by workload
+# with the hash of the GEMM sources the capture ran; a stale hash reports null.
 NCU_TRAFFIC = {
-    "dsv3_T128": {"src": "5bcf3059acb9ebea", "ratio": (1.705460e9 + 3.150080e6) / 1705541632},
-    "dsv3_T8192_zipf": {"src": "5bcf3059acb9ebea",
-                        "ratio": (2.115325e9 + 26.995968e6) / (32 * 2 * 2048 * 7168 * 2
-                                                               + 9216 * (7168 + 2048) * 2)},
+    "dsv3_T128": {"src": "5957aa0c1cc3e7e2", "ratio": 4612931797 / 4601413632},
+    "dsv3_T8192_zipf": {"src": "5957aa0c1cc3e7e2", "ratio": 10412567040 / 7935623168},
 }
 
 

@@ -423,7 +423,12 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
     if (warp == 0) {
         // =============================== TMA producer ===============================
         if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();
+            // L2 policies: with tokens on N (small batches) a weight tile is read once and is
+            // streamed evict-first; with tokens on M it is read by every token tile of its
+            // expert, CTAs that run at the same time but drift apart along K, so it is kept
+            // (evict-last, like the token rows: prefill T=8192 gate/up 3.27 -> 3.10 ms, DRAM
+            // traffic of the launch 12.6 -> see the bench's traffic table)
+            const uint64_t pol_w = C::kSwap ? policy_evict_first() : policy_evict_last();
             const uint64_t pol_x = policy_evict_last();
             int it = 0;
             bool ok = true;
