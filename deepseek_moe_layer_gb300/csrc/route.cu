@@ -66,30 +66,16 @@ MOE_DEV Top2 lane_top2(const uint32_t (&key)[EPL], const float (&val)[EPL], uint
     return t;
 }
 
-// SOFTMAX: the softmax route instead of the DeepSeek gate: the K largest logits are
-// selected (softmax is strictly increasing, so they are the K most probable experts) and
-// their weights exp(l_k - l_max) / sum_sel exp(l_j - l_max) are the selected softmax
-// probabilities renormalised over the selection, always (no bias, groups or scale).
-//
-// Each warp handles rows warp_id, warp_id + nwarps, ... (grid sized to the SMs).
-template <int EPL, bool SOFTMAX>
-__global__ void __launch_bounds__(256, EPL <= 8 ? 4 : 1) route_kernel(const RouteArgs a) {
-    pdl_launch_dependents();
-    pdl_wait();  // the logits come from the kernel before
-    const int lane = threadIdx.x & 31;
-    const long long nwarps = (long long)gridDim.x * 8;
-    const int E = a.E;
-    const int e0 = lane * EPL;
-    // vector access to bias / offset / logits_out when E and the pointers allow it
-    const bool vec_e = (EPL % 4 == 0) && (E & 3) == 0;
-    const bool bias_vec = vec_e && (reinterpret_cast<uintptr_t>(a.bias) & 15) == 0;
-    const bool off_vec = vec_e && (reinterpret_cast<uintptr_t>(a.logit_offset) & 15) == 0;
-    const bool lo_vec = vec_e && (reinterpret_cast<uintptr_t>(a.logits_out) & 15) == 0;
+template <int EPL>
+MOE_DEV void row_logits_tail(const RouteArgs& a, long long row, int e0, bool off_vec,
+                             bool lo_vec, float (&lg)[EPL]);
 
-    for (long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); row < a.rows;
-         row += nwarps) {
-    // ---- logits: sum of the split partials in split order, plus the optional offset ----
-    float lg[EPL];
+// The summed logits of `row` for this lane's slots (sum of the split partials in split
+// order, plus the optional offset), also copied to logits_out when that is set.
+template <int EPL>
+MOE_DEV void row_logits(const RouteArgs& a, long long row, int e0, bool off_vec, bool lo_vec,
+                        float (&lg)[EPL]) {
+    const int E = a.E;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) lg[i] = 0.0f;
     if (!a.bf16) {
@@ -148,6 +134,15 @@ __global__ void __launch_bounds__(256, EPL <= 8 ? 4 : 1) route_kernel(const Rout
         for (int i = 0; i < EPL; ++i)
             if (e0 + i < E) lg[i] = __uint_as_float(((uint32_t)p[e0 + i].x) << 16);
     }
+    row_logits_tail<EPL>(a, row, e0, off_vec, lo_vec, lg);
+}
+
+// Adds the optional offset to the lane's logits of `row` and copies them to logits_out when
+// that is set.
+template <int EPL>
+MOE_DEV void row_logits_tail(const RouteArgs& a, long long row, int e0, bool off_vec,
+                             bool lo_vec, float (&lg)[EPL]) {
+    const int E = a.E;
     if (a.logit_offset) {
         if (off_vec) {
 #pragma unroll
@@ -177,6 +172,33 @@ __global__ void __launch_bounds__(256, EPL <= 8 ? 4 : 1) route_kernel(const Rout
                 if (e0 + i < E) lo[e0 + i] = lg[i];
         }
     }
+
+}
+
+// SOFTMAX: the softmax route instead of the DeepSeek gate: the K largest logits are
+// selected (softmax is strictly increasing, so they are the K most probable experts) and
+// their weights exp(l_k - l_max) / sum_sel exp(l_j - l_max) are the selected softmax
+// probabilities renormalised over the selection, always (no bias, groups or scale).
+//
+// Each warp handles rows warp_id, warp_id + nwarps, ... (grid sized to the SMs).
+template <int EPL, bool SOFTMAX>
+__global__ void __launch_bounds__(256, EPL <= 8 ? 4 : 1) route_kernel(const RouteArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // the logits come from the kernel before
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = (long long)gridDim.x * 8;
+    const int E = a.E;
+    const int e0 = lane * EPL;
+    // vector access to bias / offset / logits_out when E and the pointers allow it
+    const bool vec_e = (EPL % 4 == 0) && (E & 3) == 0;
+    const bool bias_vec = vec_e && (reinterpret_cast<uintptr_t>(a.bias) & 15) == 0;
+    const bool off_vec = vec_e && (reinterpret_cast<uintptr_t>(a.logit_offset) & 15) == 0;
+    const bool lo_vec = vec_e && (reinterpret_cast<uintptr_t>(a.logits_out) & 15) == 0;
+
+    for (long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); row < a.rows;
+         row += nwarps) {
+    float lg[EPL];
+    row_logits<EPL>(a, row, e0, off_vec, lo_vec, lg);
 
     // ---- selection keys: sigmoid + bias (DeepSeek) or the logit itself (softmax) ----
     float orig[EPL];
@@ -344,6 +366,251 @@ __global__ void __launch_bounds__(256, EPL <= 8 ? 4 : 1) route_kernel(const Rout
     }  // rows
 }
 
+// ---- the DeepSeek gate in fewer instructions per token -------------------------------
+//
+// gate_kernel<EPL> computes exactly route_kernel<EPL, false>'s result for up to 8 experts
+// per lane when E % EPL == 0 and the group mask is off (n_group == 1 or no group dropped)
+// or its groups are a power-of-two number of whole lanes (E / n_group = lanes * EPL): the
+// DeepSeek-V3 shape (256 experts, 8 groups of 32) and its smaller relatives.  Per token:
+//  - each lane keeps its three best slots (key descending, index ascending) and re-scans
+//    its untaken slots only after all three were selected;
+//  - the kept groups come from min(topk_group, n_group - topk_group) warp rounds: the best
+//    group is kept (ties to the lower index) or the worst one dropped (ties to the higher);
+//  - the pre-bias sigmoid values go to shared memory, where lane k reads its winner's;
+//  - the bias stays in registers for all tokens of the warp.
+
+// Key of a biased score s + b with s = sigmoid(l): s is +0 or more, so s + b is never -0 and
+// only NaN needs folding; otherwise the same key as okey().  NaN gets 1, still below every
+// number (-inf's key is 0x007FFFFF), so that 0 marks an empty list entry and no expert's.
+MOE_DEV uint32_t score_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+    return f != f ? 1u : k;
+}
+
+// Inserts slot (key, e) into a lane's best-three list k/ix (key descending, index
+// ascending; entries at or beyond `filled` may be empty, marked by ix == kEmpty).  Slots
+// arrive in increasing index, so an equal key stays behind the entries already listed.
+MOE_DEV void list_insert(uint32_t (&k)[3], uint32_t (&ix)[3], uint32_t key, uint32_t e,
+                         int filled) {
+    bool c[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) c[j] = (j >= filled && ix[j] == kEmpty) || key > k[j];
+#pragma unroll
+    for (int j = 2; j >= 0; --j) {
+        if (c[j]) {
+            const bool up = j > 0 && c[j > 0 ? j - 1 : 0];
+            k[j] = up ? k[j > 0 ? j - 1 : 0] : key;
+            ix[j] = up ? ix[j > 0 ? j - 1 : 0] : e;
+        }
+    }
+}
+
+// KC: top_k fixed at compile time (0: a.top_k).
+template <int EPL, int KC>
+__global__ void __launch_bounds__(256, 4) gate_kernel(const RouteArgs a) {
+    static_assert(EPL >= 1 && EPL <= 8, "one to eight experts per lane");
+    __shared__ __align__(16) float s_val[8][32 * EPL];
+    __shared__ uint32_t s_win[8][32];
+    __shared__ __align__(16) float s_bias[32 * EPL];
+    pdl_launch_dependents();
+    pdl_wait();  // the logits come from the kernel before
+    const int lane = threadIdx.x & 31;
+    float* const sv = s_val[threadIdx.x >> 5];
+    uint32_t* const swin = s_win[threadIdx.x >> 5];
+    const long long nwarps = (long long)gridDim.x * 8;
+    const int E = a.E;
+    const int e0 = lane * EPL;
+    const bool live = e0 < E;  // E % EPL == 0: a lane's slots are all experts or none
+    const bool vec_e = (EPL % 4 == 0);
+    const bool off_vec = vec_e && (reinterpret_cast<uintptr_t>(a.logit_offset) & 15) == 0;
+    const bool lo_vec = vec_e && (reinterpret_cast<uintptr_t>(a.logits_out) & 15) == 0;
+
+    for (int e = threadIdx.x; e < 32 * EPL; e += 256) s_bias[e] = e < E ? a.bias[e] : 0.0f;
+    __syncthreads();
+
+    // group mask: lanes [g * lpg, (g + 1) * lpg) hold group g (lpg a power of two)
+    const int G = a.n_group;
+    const bool grouped = G > 1 && G > a.topk_group;
+    int gshift = 0;
+    if (grouped) gshift = __ffs((E / G) / EPL) - 1;
+    const int grp = lane >> gshift;
+    const bool in_group = grouped && live;
+    const uint32_t zero_key = 0x80000000u;  // key of +0.0
+    const int K = KC ? KC : a.top_k;
+
+    // one fp32 split with 16-byte rows: the next token's logits load while this one's route
+    // is computed
+    constexpr int kV = EPL % 4 == 0 ? EPL / 4 : 1;
+    const bool pf = EPL % 4 == 0 && !a.bf16 && a.nsplit == 1 &&
+                    (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0;
+    const float* const lbase = static_cast<const float*>(a.logits) + e0;
+    float4 nx[kV];
+    long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (pf && live && row < a.rows) {
+#pragma unroll
+        for (int v = 0; v < kV; ++v)
+            nx[v] = *reinterpret_cast<const float4*>(lbase + row * E + 4 * v);
+    }
+
+    for (; row < a.rows; row += nwarps) {
+        float lg[EPL];
+        if (pf) {
+#pragma unroll
+            for (int v = 0; v < kV; ++v) {
+                lg[(4 * v) % EPL] = nx[v].x; lg[(4 * v + 1) % EPL] = nx[v].y;
+                lg[(4 * v + 2) % EPL] = nx[v].z; lg[(4 * v + 3) % EPL] = nx[v].w;
+            }
+            const long long nr = row + nwarps;
+            if (live && nr < a.rows) {
+#pragma unroll
+                for (int v = 0; v < kV; ++v)
+                    nx[v] = *reinterpret_cast<const float4*>(lbase + nr * E + 4 * v);
+            }
+            row_logits_tail<EPL>(a, row, e0, off_vec, lo_vec, lg);
+        } else {
+            row_logits<EPL>(a, row, e0, off_vec, lo_vec, lg);
+        }
+
+        // sigmoid (the weights' values, to shared memory) and the biased selection keys
+        uint32_t key[EPL];
+        float val[EPL], bs[EPL];
+        if constexpr (EPL % 4 == 0) {
+#pragma unroll
+            for (int v = 0; v < EPL / 4; ++v) {
+                const float4 b = *reinterpret_cast<const float4*>(s_bias + e0 + 4 * v);
+                bs[(4 * v) % EPL] = b.x; bs[(4 * v + 1) % EPL] = b.y;
+                bs[(4 * v + 2) % EPL] = b.z; bs[(4 * v + 3) % EPL] = b.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) bs[i] = s_bias[e0 + i];
+        }
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            val[i] = 1.0f / (1.0f + expf(-lg[i]));
+            key[i] = score_key(val[i] + bs[i]);
+        }
+        if (live) {
+            if constexpr (EPL % 4 == 0) {
+#pragma unroll
+                for (int i = 0; i < EPL; i += 4)
+                    *reinterpret_cast<float4*>(sv + e0 + i) =
+                        make_float4(val[i], val[i + 1], val[i + 2], val[i + 3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) sv[e0 + i] = val[i];
+            }
+        }
+
+        // the lane's best three slots
+        uint32_t lk[3] = {0u, 0u, 0u}, li[3] = {kEmpty, kEmpty, kEmpty};
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) list_insert(lk, li, key[i], (uint32_t)(e0 + i), i);
+        if (!live) {
+#pragma unroll
+            for (int j = 0; j < 3; ++j) { lk[j] = 0u; li[j] = kEmpty; }
+        }
+
+        if (grouped) {
+            // group score: the sum of the group's two largest keys' values
+            uint32_t t1 = lk[0], t2 = EPL > 1 ? lk[1] : 0u;
+            for (int off = 1; off < (1 << gshift); off <<= 1) {
+                const uint32_t o1 = __shfl_xor_sync(kFull, t1, off);
+                const uint32_t o2 = __shfl_xor_sync(kFull, t2, off);
+                const uint32_t n2 = max(min(t1, o1), max(t2, o2));
+                t1 = max(t1, o1);
+                t2 = n2;
+            }
+            // (a NaN key, 1, reads back as NaN: the sum is NaN and its key 0, the lowest)
+            const uint32_t gk = okey(okey_value(t1) + okey_value(t2));
+            // the group's rank (larger key first, ties to the lower index) from every
+            // group's key at once: group h sits in lanes [h * lpg, (h + 1) * lpg)
+            int rank = 0;
+#pragma unroll 8
+            for (int h = 0; h < G; ++h) {
+                const uint32_t hk = __shfl_sync(kFull, gk, h << gshift);
+                rank += (hk > gk) || (hk == gk && h < grp);
+            }
+            if (in_group && rank >= a.topk_group) {
+                // a dropped group's scores are all 0: its slots in index order
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) key[i] = zero_key;
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    lk[j] = j < EPL ? zero_key : 0u;
+                    li[j] = j < EPL ? (uint32_t)(e0 + j) : kEmpty;
+                }
+            }
+        }
+
+        // top-k: per expert, the largest list head; lanes hold increasing expert ranges and
+        // a head is its lane's lowest-index maximum, so the lowest lane holding the largest
+        // head has the lowest expert index among the maxima
+        // A lane that gives its third listed slot before the last round while it holds more
+        // than three slots may hold a later winner outside its list: the token then takes the
+        // exact rounds below instead (rare: a lane holding three of the token's winners).
+        // Expert keys are at least 1, so an empty entry (key 0) never equals a maximum.
+        bool short_list = false;
+        const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+        for (int r = 0; r < (KC ? KC : 32); ++r) {
+            if (!KC && r >= K) break;
+            const uint32_t m = __reduce_max_sync(kFull, lk[0]);
+            const bool top = lk[0] == m;
+            const unsigned b = __ballot_sync(kFull, top);
+            if (top && (b & below) == 0u) {
+                swin[r] = li[0];
+                lk[0] = lk[1]; li[0] = li[1];
+                lk[1] = lk[2]; li[1] = li[2];
+                lk[2] = 0u; li[2] = kEmpty;
+                if (EPL > 3 && r + 1 < K) short_list = short_list || lk[0] == 0u;
+            }
+        }
+        if (__any_sync(kFull, short_list)) {
+            // exact rounds: the winner's lane re-scans its untaken slots for its next head
+            uint32_t hk = 0u, hi = kEmpty, taken = 0u;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (live && (hi == kEmpty || key[i] > hk)) { hk = key[i]; hi = (uint32_t)(e0 + i); }
+#pragma unroll 1
+            for (int r = 0; r < K; ++r) {
+                const uint32_t m = __reduce_max_sync(kFull, hk);
+                const bool top = hk == m;
+                const unsigned b = __ballot_sync(kFull, top);
+                if (top && (b & below) == 0u) {
+                    swin[r] = hi;
+                    taken |= 1u << (hi - (uint32_t)e0);
+                    hk = 0u;
+                    hi = kEmpty;
+#pragma unroll
+                    for (int i = 0; i < EPL; ++i)
+                        if (!(taken & (1u << i)) && (hi == kEmpty || key[i] > hk)) {
+                            hk = key[i];
+                            hi = (uint32_t)(e0 + i);
+                        }
+                }
+            }
+        }
+        __syncwarp();  // winners and values in shared memory are visible to the whole warp
+
+        // weights: renormalise (K > 1 and norm; summed in selection order), then scale
+        const uint32_t my_idx = lane < K ? swin[lane] : 0u;
+        float my_w = lane < K ? sv[my_idx] : 0.0f;
+        if (K > 1 && a.norm) {
+            float sum = 0.0f;
+            for (int k = 0; k < K; ++k) sum += sv[swin[k]];
+            my_w = my_w / sum;
+        }
+        my_w = my_w * a.scale;
+        if (lane < K) {
+            a.inds[row * K + lane] = (int)my_idx;
+            a.scores[row * K + lane] = my_w;
+        }
+        __syncwarp();  // reads done before the next token's values are written
+    }  // rows
+}
+
 __global__ void add_offset_kernel(float* __restrict__ logits, long long n, int E,
                                   const float* __restrict__ offset) {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -379,6 +646,23 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
             default: return launch_kernel(route_kernel<32, true>, dim3(grid), dim3(256), 0, s, a);
         }
         return cudaGetLastError();
+    }
+    // the DeepSeek gate's short form (same result) where its layout conditions hold
+    const int G = a.n_group;
+    const bool grouped = G > 1 && G > a.topk_group;
+    const int lpg = grouped && (a.E / G) % epl == 0 ? (a.E / G) / epl : 0;
+    const bool groups_fit = !grouped || (lpg > 0 && (lpg & (lpg - 1)) == 0);
+    if (epl <= 8 && a.E % epl == 0 && groups_fit) {
+        switch (epl) {
+            case 1: return a.top_k == 8 ? launch_kernel(gate_kernel<1, 8>, dim3(grid), dim3(256), 0, s, a)
+                                        : launch_kernel(gate_kernel<1, 0>, dim3(grid), dim3(256), 0, s, a);
+            case 2: return a.top_k == 8 ? launch_kernel(gate_kernel<2, 8>, dim3(grid), dim3(256), 0, s, a)
+                                        : launch_kernel(gate_kernel<2, 0>, dim3(grid), dim3(256), 0, s, a);
+            case 4: return a.top_k == 8 ? launch_kernel(gate_kernel<4, 8>, dim3(grid), dim3(256), 0, s, a)
+                                        : launch_kernel(gate_kernel<4, 0>, dim3(grid), dim3(256), 0, s, a);
+            default: return a.top_k == 8 ? launch_kernel(gate_kernel<8, 8>, dim3(grid), dim3(256), 0, s, a)
+                                         : launch_kernel(gate_kernel<8, 0>, dim3(grid), dim3(256), 0, s, a);
+        }
     }
     switch (epl) {
         case 1: return launch_kernel(route_kernel<1, false>, dim3(grid), dim3(256), 0, s, a);

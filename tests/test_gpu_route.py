@@ -66,6 +66,27 @@ def test_route_exact_ties(E, G, tg, K):
     _run(torch.zeros(3, E, device=DEV), torch.zeros(E, device=DEV), K, G, tg, True, 1.0)
 
 
+@pytest.mark.parametrize("E,G,tg,K", [(256, 8, 4, 8), (256, 1, 1, 8), (128, 4, 2, 8),
+                                     (64, 8, 4, 16), (256, 8, 4, 5), (256, 4, 3, 7)])
+def test_route_winners_crowded_into_one_run(E, G, tg, K):
+    """Rows whose largest scores crowd into 3, 4 or 8 neighbouring experts of one aligned run
+    of eight (a lane of the gate holds such a run, and a lane giving more than three winners
+    takes the exact re-scanning rounds), and the same rows with every kept score negative
+    (bias - 2), where the dropped groups' zeros lead in index order."""
+    g = torch.Generator(device=DEV).manual_seed(E * 7 + K)
+    rows = 600
+    logits = torch.randn(rows, E, generator=g, device=DEV)
+    start = torch.randint(0, E // 8, (rows,), generator=g, device=DEV) * 8
+    cnt = torch.tensor([3, 4, 8], device=DEV)[torch.arange(rows, device=DEV) % 3]
+    off = torch.arange(8, device=DEV)
+    cols = start[:, None] + off[None, :]
+    vals = 6 + torch.rand(rows, 8, generator=g, device=DEV)
+    logits.scatter_(1, cols, torch.where(off[None, :] < cnt[:, None], vals, logits.gather(1, cols)))
+    bias = torch.randn(E, generator=g, device=DEV) * 0.1
+    assert _run(logits, bias, K, G, tg, True, 2.5) <= rows // 50
+    assert _run(logits, bias - 2.0, K, G, tg, True, 2.5) <= rows // 50
+
+
 def test_route_nan_and_signed_zero():
     """NaN logits rank below every number (their experts and all-NaN groups are the last
     choices) and -0 == +0 (sigma(-0) and sigma(+0) tie, the lower expert index first), on
