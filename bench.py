@@ -254,7 +254,7 @@ def time_routing(dev, replays=50):
     torch.cuda.empty_cache()
     return {"workload": f"routing_{rows}x{E}", "l2": "16 rotating copies of the logits "
             "(269 MB > L2); launches replayed from a CUDA graph",
-            "kernel": "route_kernel<8, false>", **out}
+            "kernel": "gate_kernel<8, 8, GC, 32> (GC = 8 grouped, 0 flat)", **out}
 
 
 def time_indexer(dev, reps=20):

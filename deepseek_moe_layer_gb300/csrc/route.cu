@@ -68,13 +68,13 @@ MOE_DEV Top2 lane_top2(const uint32_t (&key)[EPL], const float (&val)[EPL], uint
 
 template <int EPL>
 MOE_DEV void row_logits_tail(const RouteArgs& a, long long row, int e0, bool off_vec,
-                             bool lo_vec, float (&lg)[EPL]);
+                             bool lo_vec, bool lo_write, float (&lg)[EPL]);
 
 // The summed logits of `row` for this lane's slots (sum of the split partials in split
 // order, plus the optional offset), also copied to logits_out when that is set.
 template <int EPL>
 MOE_DEV void row_logits(const RouteArgs& a, long long row, int e0, bool off_vec, bool lo_vec,
-                        float (&lg)[EPL]) {
+                        bool lo_write, float (&lg)[EPL]) {
     const int E = a.E;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) lg[i] = 0.0f;
@@ -134,14 +134,14 @@ MOE_DEV void row_logits(const RouteArgs& a, long long row, int e0, bool off_vec,
         for (int i = 0; i < EPL; ++i)
             if (e0 + i < E) lg[i] = __uint_as_float(((uint32_t)p[e0 + i].x) << 16);
     }
-    row_logits_tail<EPL>(a, row, e0, off_vec, lo_vec, lg);
+    row_logits_tail<EPL>(a, row, e0, off_vec, lo_vec, lo_write, lg);
 }
 
 // Adds the optional offset to the lane's logits of `row` and copies them to logits_out when
 // that is set.
 template <int EPL>
 MOE_DEV void row_logits_tail(const RouteArgs& a, long long row, int e0, bool off_vec,
-                             bool lo_vec, float (&lg)[EPL]) {
+                             bool lo_vec, bool lo_write, float (&lg)[EPL]) {
     const int E = a.E;
     if (a.logit_offset) {
         if (off_vec) {
@@ -158,7 +158,7 @@ MOE_DEV void row_logits_tail(const RouteArgs& a, long long row, int e0, bool off
                 if (e0 + i < E) lg[i] = lg[i] + a.logit_offset[e0 + i];
         }
     }
-    if (a.logits_out) {
+    if (a.logits_out && lo_write) {
         float* lo = a.logits_out + row * E;
         if (lo_vec) {
 #pragma unroll
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(256, EPL <= 8 ? 4 : 1) route_kernel(const Rout
     for (long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); row < a.rows;
          row += nwarps) {
     float lg[EPL];
-    row_logits<EPL>(a, row, e0, off_vec, lo_vec, lg);
+    row_logits<EPL>(a, row, e0, off_vec, lo_vec, true, lg);
 
     // ---- selection keys: sigmoid + bias (DeepSeek) or the logit itself (softmax) ----
     float orig[EPL];
@@ -368,16 +368,18 @@ __global__ void __launch_bounds__(256, EPL <= 8 ? 4 : 1) route_kernel(const Rout
 
 // ---- the DeepSeek gate in fewer instructions per token -------------------------------
 //
-// gate_kernel<EPL> computes exactly route_kernel<EPL, false>'s result for up to 8 experts
-// per lane when E % EPL == 0 and the group mask is off (n_group == 1 or no group dropped)
-// or its groups are a power-of-two number of whole lanes (E / n_group = lanes * EPL): the
-// DeepSeek-V3 shape (256 experts, 8 groups of 32) and its smaller relatives.  Per token:
-//  - each lane keeps its three best slots (key descending, index ascending) and re-scans
-//    its untaken slots only after all three were selected;
-//  - the kept groups come from min(topk_group, n_group - topk_group) warp rounds: the best
-//    group is kept (ties to the lower index) or the worst one dropped (ties to the higher);
-//  - the pre-bias sigmoid values go to shared memory, where lane k reads its winner's;
-//  - the bias stays in registers for all tokens of the warp.
+// gate_kernel computes exactly route_kernel<.., false>'s result (the same K experts in the
+// same order, weights summed in that order) for up to 8 experts per lane when E % EPL == 0
+// and the group mask is off (n_group == 1 or no group dropped) or its groups are a
+// power-of-two number of whole lanes: the DeepSeek-V3 shape (256 experts, 8 groups of 32)
+// and its relatives.  One warp routes a token; lane l holds experts [l * EPL, l * EPL + EPL).
+//  - each lane lists its three best slots (key descending, index ascending) and its
+//    fourth-best key; if that fourth entry wins a round (four of the K winners in one lane,
+//    rare), the token is redone by exact rounds that re-scan the winner's lane;
+//  - the group mask ranks every group's key at once;
+//  - the pre-bias sigmoid values and the winners go to shared memory, where lane k reads
+//    the k-th winner's value and every lane sums the K values in selection order;
+//  - the next token's logits load while this one is routed.
 
 // Key of a biased score s + b with s = sigmoid(l): s is +0 or more, so s + b is never -0 and
 // only NaN needs folding; otherwise the same key as okey().  NaN gets 1, still below every
@@ -388,14 +390,18 @@ MOE_DEV uint32_t score_key(float f) {
     return f != f ? 1u : k;
 }
 
-// Inserts slot (key, e) into a lane's best-three list k/ix (key descending, index
-// ascending; entries at or beyond `filled` may be empty, marked by ix == kEmpty).  Slots
-// arrive in increasing index, so an equal key stays behind the entries already listed.
-MOE_DEV void list_insert(uint32_t (&k)[3], uint32_t (&ix)[3], uint32_t key, uint32_t e,
+constexpr uint32_t kBound = 0xFFFFFFFEu;  // list entry holding the fourth-best key only
+
+// Inserts slot (key, e) into a lane's list: its best three slots k[0..2] / ix[0..2] (key
+// descending, index ascending; an entry at or beyond `filled` may be empty, ix == kEmpty,
+// k == 0) and the largest key below them, k[3] (0: none).  Slots arrive in increasing
+// index, so an equal key stays behind the entries already listed.
+MOE_DEV void list_insert(uint32_t (&k)[4], uint32_t (&ix)[3], uint32_t key, uint32_t e,
                          int filled) {
     bool c[3];
 #pragma unroll
     for (int j = 0; j < 3; ++j) c[j] = (j >= filled && ix[j] == kEmpty) || key > k[j];
+    k[3] = max(k[3], c[2] ? k[2] : key);  // the slot that leaves (or misses) the best three
 #pragma unroll
     for (int j = 2; j >= 0; --j) {
         if (c[j]) {
@@ -406,54 +412,106 @@ MOE_DEV void list_insert(uint32_t (&k)[3], uint32_t (&ix)[3], uint32_t key, uint
     }
 }
 
-// KC: top_k fixed at compile time (0: a.top_k).
-template <int EPL, int KC>
-__global__ void __launch_bounds__(256, 4) gate_kernel(const RouteArgs a) {
+// One selection round over the lanes' list heads.  The owner is the lowest lane holding the
+// largest head (lanes hold increasing expert ranges and a head is its lane's lowest-index
+// maximum, so that is the lowest expert index among the maxima; expert keys are at least 1,
+// so an empty entry, key 0, never equals the maximum).  The owner writes its head's index
+// to `win` (a shared-memory address), notes in `redo` a fourth-best entry taken, and pops:
+// its list moves up and the third place takes the fourth-best key with index kBound.
+// Written predicated, without a branch, as the round is the token's critical path.
+MOE_DEV void select_round(uint32_t (&k)[4], uint32_t (&ix)[3], uint32_t below, uint32_t win,
+                          uint32_t& redo) {
+    asm volatile(
+        "{\n\t"
+        ".reg .u32 m, b, t;\n\t"
+        ".reg .pred top, own, bnd;\n\t"
+        "redux.sync.max.u32 m, %0, 0xffffffff;\n\t"
+        "setp.eq.u32 top, %0, m;\n\t"
+        "vote.sync.ballot.b32 b, top, 0xffffffff;\n\t"
+        "and.b32 t, b, %8;\n\t"
+        "setp.eq.and.u32 own, t, 0, top;\n\t"
+        "@own st.shared.u32 [%9], %4;\n\t"
+        "setp.eq.and.u32 bnd, %4, %10, own;\n\t"
+        "@bnd mov.u32 %7, 1;\n\t"
+        "@own mov.u32 %0, %1;\n\t"
+        "@own mov.u32 %1, %2;\n\t"
+        "@own mov.u32 %2, %3;\n\t"
+        "@own mov.u32 %3, 0;\n\t"
+        "@own mov.u32 %4, %5;\n\t"
+        "@own mov.u32 %5, %6;\n\t"
+        "@own mov.u32 %6, %10;\n\t"
+        "}"
+        : "+r"(k[0]), "+r"(k[1]), "+r"(k[2]), "+r"(k[3]), "+r"(ix[0]), "+r"(ix[1]),
+          "+r"(ix[2]), "+r"(redo)
+        : "r"(below), "r"(win), "n"(kBound)
+        : "memory");
+}
+
+constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
+
+// KC: top_k fixed at compile time (0: a.top_k).  GC: n_group fixed at compile time with
+// E == 32 * EPL (0: from the arguments).  NW: warps per CTA.  CTA c routes tokens
+// [c * rows / grid, (c + 1) * rows / grid), its warps taking one token at a time from a
+// shared-memory counter, so that every warp of an SM stays busy until the SM's tokens run
+// out (warps given fixed shares finish at very different times: the scheduler favours the
+// older ones).
+template <int EPL, int KC, int GC, int NW>
+__global__ void __launch_bounds__(NW * 32, NW >= 16 ? 1 : 4) gate_kernel(const RouteArgs a) {
     static_assert(EPL >= 1 && EPL <= 8, "one to eight experts per lane");
-    __shared__ __align__(16) float s_val[8][32 * EPL];
-    __shared__ uint32_t s_win[8][32];
-    __shared__ __align__(16) float s_bias[32 * EPL];
+    constexpr int kNE = 32 * EPL;  // expert slots of a token
+    __shared__ __align__(16) float s_val[NW][kNE];
+    __shared__ uint32_t s_win[NW][32];
+    __shared__ __align__(16) float s_bias[kNE];
+    __shared__ int s_next;
     pdl_launch_dependents();
     pdl_wait();  // the logits come from the kernel before
     const int lane = threadIdx.x & 31;
     float* const sv = s_val[threadIdx.x >> 5];
     uint32_t* const swin = s_win[threadIdx.x >> 5];
-    const long long nwarps = (long long)gridDim.x * 8;
-    const int E = a.E;
+    const uint32_t swin_s = (uint32_t)__cvta_generic_to_shared(swin);
+    const int E = GC ? kNE : a.E;
     const int e0 = lane * EPL;
     const bool live = e0 < E;  // E % EPL == 0: a lane's slots are all experts or none
     const bool vec_e = (EPL % 4 == 0);
     const bool off_vec = vec_e && (reinterpret_cast<uintptr_t>(a.logit_offset) & 15) == 0;
     const bool lo_vec = vec_e && (reinterpret_cast<uintptr_t>(a.logits_out) & 15) == 0;
-
-    for (int e = threadIdx.x; e < 32 * EPL; e += 256) s_bias[e] = e < E ? a.bias[e] : 0.0f;
+    for (int e = threadIdx.x; e < kNE; e += NW * 32) s_bias[e] = e < E ? a.bias[e] : 0.0f;
+    if (threadIdx.x == 0) s_next = 0;
     __syncthreads();
 
     // group mask: lanes [g * lpg, (g + 1) * lpg) hold group g (lpg a power of two)
-    const int G = a.n_group;
-    const bool grouped = G > 1 && G > a.topk_group;
-    int gshift = 0;
-    if (grouped) gshift = __ffs((E / G) / EPL) - 1;
+    const int G = GC ? GC : a.n_group;
+    const bool grouped = GC ? true : (G > 1 && G > a.topk_group);
+    int gshift = GC ? ilog2(32 / (GC ? GC : 1)) : 0;
+    if (!GC && grouped) gshift = __ffs((E / G) / EPL) - 1;
     const int grp = lane >> gshift;
     const bool in_group = grouped && live;
     const uint32_t zero_key = 0x80000000u;  // key of +0.0
     const int K = KC ? KC : a.top_k;
+    const uint32_t below = (1u << lane) - 1u;
 
-    // one fp32 split with 16-byte rows: the next token's logits load while this one's route
-    // is computed
+    // one fp32 split with 16-byte rows: the next token's logits load while this one is routed
     constexpr int kV = EPL % 4 == 0 ? EPL / 4 : 1;
     const bool pf = EPL % 4 == 0 && !a.bf16 && a.nsplit == 1 &&
                     (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0;
     const float* const lbase = static_cast<const float*>(a.logits) + e0;
+    const long long lo = a.rows * blockIdx.x / gridDim.x;
+    const long long hi = a.rows * (blockIdx.x + 1) / gridDim.x;
+    auto take = [&]() -> long long {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&s_next, 1);
+        return lo + __shfl_sync(kFull, t, 0);
+    };
+    long long row = take();  // the warp's first token
     float4 nx[kV];
-    long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (pf && live && row < a.rows) {
+    if (pf && live && row < hi) {
 #pragma unroll
         for (int v = 0; v < kV; ++v)
             nx[v] = *reinterpret_cast<const float4*>(lbase + row * E + 4 * v);
     }
 
-    for (; row < a.rows; row += nwarps) {
+    while (row < hi) {
+        const long long next = take();  // loaded while this token is routed
         float lg[EPL];
         if (pf) {
 #pragma unroll
@@ -461,15 +519,14 @@ __global__ void __launch_bounds__(256, 4) gate_kernel(const RouteArgs a) {
                 lg[(4 * v) % EPL] = nx[v].x; lg[(4 * v + 1) % EPL] = nx[v].y;
                 lg[(4 * v + 2) % EPL] = nx[v].z; lg[(4 * v + 3) % EPL] = nx[v].w;
             }
-            const long long nr = row + nwarps;
-            if (live && nr < a.rows) {
+            if (live && next < hi) {
 #pragma unroll
                 for (int v = 0; v < kV; ++v)
-                    nx[v] = *reinterpret_cast<const float4*>(lbase + nr * E + 4 * v);
+                    nx[v] = *reinterpret_cast<const float4*>(lbase + next * E + 4 * v);
             }
-            row_logits_tail<EPL>(a, row, e0, off_vec, lo_vec, lg);
+            row_logits_tail<EPL>(a, row, e0, off_vec, lo_vec, true, lg);
         } else {
-            row_logits<EPL>(a, row, e0, off_vec, lo_vec, lg);
+            row_logits<EPL>(a, row, e0, off_vec, lo_vec, true, lg);
         }
 
         // sigmoid (the weights' values, to shared memory) and the biased selection keys
@@ -503,32 +560,36 @@ __global__ void __launch_bounds__(256, 4) gate_kernel(const RouteArgs a) {
             }
         }
 
-        // the lane's best three slots
-        uint32_t lk[3] = {0u, 0u, 0u}, li[3] = {kEmpty, kEmpty, kEmpty};
+        // the lane's best three slots and fourth-best key
+        uint32_t lk[4] = {0u, 0u, 0u, 0u}, li[3] = {kEmpty, kEmpty, kEmpty};
 #pragma unroll
         for (int i = 0; i < EPL; ++i) list_insert(lk, li, key[i], (uint32_t)(e0 + i), i);
         if (!live) {
 #pragma unroll
             for (int j = 0; j < 3; ++j) { lk[j] = 0u; li[j] = kEmpty; }
+            lk[3] = 0u;
         }
 
         if (grouped) {
-            // group score: the sum of the group's two largest keys' values
+            // group score: the sum of the group's two largest keys' values (a NaN key, 1,
+            // reads back as NaN: the sum is NaN and its key 0, the lowest)
             uint32_t t1 = lk[0], t2 = EPL > 1 ? lk[1] : 0u;
-            for (int off = 1; off < (1 << gshift); off <<= 1) {
+#pragma unroll
+            for (int off = 1; off < (GC ? 32 / (GC ? GC : 1) : 32); off <<= 1) {
+                if (!GC && off >= (1 << gshift)) break;
                 const uint32_t o1 = __shfl_xor_sync(kFull, t1, off);
                 const uint32_t o2 = __shfl_xor_sync(kFull, t2, off);
                 const uint32_t n2 = max(min(t1, o1), max(t2, o2));
                 t1 = max(t1, o1);
                 t2 = n2;
             }
-            // (a NaN key, 1, reads back as NaN: the sum is NaN and its key 0, the lowest)
             const uint32_t gk = okey(okey_value(t1) + okey_value(t2));
             // the group's rank (larger key first, ties to the lower index) from every
-            // group's key at once: group h sits in lanes [h * lpg, (h + 1) * lpg)
+            // group's key at once
             int rank = 0;
-#pragma unroll 8
-            for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int h = 0; h < (GC ? GC : 32); ++h) {
+                if (!GC && h >= G) break;
                 const uint32_t hk = __shfl_sync(kFull, gk, h << gshift);
                 rank += (hk > gk) || (hk == gk && h < grp);
             }
@@ -541,53 +602,38 @@ __global__ void __launch_bounds__(256, 4) gate_kernel(const RouteArgs a) {
                     lk[j] = j < EPL ? zero_key : 0u;
                     li[j] = j < EPL ? (uint32_t)(e0 + j) : kEmpty;
                 }
+                lk[3] = EPL > 3 ? zero_key : 0u;
             }
         }
 
-        // top-k: per expert, the largest list head; lanes hold increasing expert ranges and
-        // a head is its lane's lowest-index maximum, so the lowest lane holding the largest
-        // head has the lowest expert index among the maxima
-        // A lane that gives its third listed slot before the last round while it holds more
-        // than three slots may hold a later winner outside its list: the token then takes the
-        // exact rounds below instead (rare: a lane holding three of the token's winners).
-        // Expert keys are at least 1, so an empty entry (key 0) never equals a maximum.
-        bool short_list = false;
-        const uint32_t below = (1u << lane) - 1u;
+        // top-k: K rounds over the list heads
+        uint32_t redo = 0u;
 #pragma unroll
         for (int r = 0; r < (KC ? KC : 32); ++r) {
             if (!KC && r >= K) break;
-            const uint32_t m = __reduce_max_sync(kFull, lk[0]);
-            const bool top = lk[0] == m;
-            const unsigned b = __ballot_sync(kFull, top);
-            if (top && (b & below) == 0u) {
-                swin[r] = li[0];
-                lk[0] = lk[1]; li[0] = li[1];
-                lk[1] = lk[2]; li[1] = li[2];
-                lk[2] = 0u; li[2] = kEmpty;
-                if (EPL > 3 && r + 1 < K) short_list = short_list || lk[0] == 0u;
-            }
+            select_round(lk, li, below, swin_s + 4u * r, redo);
         }
-        if (__any_sync(kFull, short_list)) {
+        if (__any_sync(kFull, redo != 0u)) {
             // exact rounds: the winner's lane re-scans its untaken slots for its next head
-            uint32_t hk = 0u, hi = kEmpty, taken = 0u;
+            uint32_t hk = 0u, hi_ = kEmpty, taken = 0u;
 #pragma unroll
             for (int i = 0; i < EPL; ++i)
-                if (live && (hi == kEmpty || key[i] > hk)) { hk = key[i]; hi = (uint32_t)(e0 + i); }
+                if (live && (hi_ == kEmpty || key[i] > hk)) { hk = key[i]; hi_ = (uint32_t)(e0 + i); }
 #pragma unroll 1
             for (int r = 0; r < K; ++r) {
                 const uint32_t m = __reduce_max_sync(kFull, hk);
                 const bool top = hk == m;
                 const unsigned b = __ballot_sync(kFull, top);
                 if (top && (b & below) == 0u) {
-                    swin[r] = hi;
-                    taken |= 1u << (hi - (uint32_t)e0);
+                    swin[r] = hi_;
+                    taken |= 1u << (hi_ - (uint32_t)e0);
                     hk = 0u;
-                    hi = kEmpty;
+                    hi_ = kEmpty;
 #pragma unroll
                     for (int i = 0; i < EPL; ++i)
-                        if (!(taken & (1u << i)) && (hi == kEmpty || key[i] > hk)) {
+                        if (!(taken & (1u << i)) && (hi_ == kEmpty || key[i] > hk)) {
                             hk = key[i];
-                            hi = (uint32_t)(e0 + i);
+                            hi_ = (uint32_t)(e0 + i);
                         }
                 }
             }
@@ -608,7 +654,8 @@ __global__ void __launch_bounds__(256, 4) gate_kernel(const RouteArgs a) {
             a.scores[row * K + lane] = my_w;
         }
         __syncwarp();  // reads done before the next token's values are written
-    }  // rows
+        row = next;
+    }  // tokens
 }
 
 __global__ void add_offset_kernel(float* __restrict__ logits, long long n, int E,
@@ -650,19 +697,33 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     // the DeepSeek gate's short form (same result) where its layout conditions hold
     const int G = a.n_group;
     const bool grouped = G > 1 && G > a.topk_group;
-    const int lpg = grouped && (a.E / G) % epl == 0 ? (a.E / G) / epl : 0;
-    const bool groups_fit = !grouped || (lpg > 0 && (lpg & (lpg - 1)) == 0);
-    if (epl <= 8 && a.E % epl == 0 && groups_fit) {
+    auto groups_fit = [&](int lanes_epl) {
+        if (!grouped) return true;
+        const int eg = a.E / G;
+        const int lpg = eg % lanes_epl == 0 ? eg / lanes_epl : 0;
+        return lpg > 0 && (lpg & (lpg - 1)) == 0;
+    };
+    // one CTA of 32 warps per SM when every warp gets a token (each CTA a contiguous token
+    // range), else CTAs of 8 warps, a token per warp
+    // one CTA of 32 warps per SM when every warp gets a token (each CTA a contiguous token
+    // range), else CTAs of 8 warps, a token per warp
+    if (epl <= 8 && a.E % epl == 0 && groups_fit(epl)) {
+        const bool wide = a.rows >= 32LL * num_sms();
+        const unsigned g32 = (unsigned)num_sms();
+        const unsigned g8 = (unsigned)((a.rows + 7) / 8);
+#define MOE_GATE(EPL_, KC_, GC_)                                                                  \
+    return wide ? launch_kernel(gate_kernel<EPL_, KC_, GC_, 32>, dim3(g32), dim3(1024), 0, s, a) \
+                : launch_kernel(gate_kernel<EPL_, KC_, GC_, 8>, dim3(g8), dim3(256), 0, s, a)
+        // the DeepSeek-V3 gate: 256 experts, 8 groups, some dropped, top-8
+        if (a.E == 256 && G == 8 && grouped && a.top_k == 8) MOE_GATE(8, 8, 8);
+        const bool k8 = a.top_k == 8;
         switch (epl) {
-            case 1: return a.top_k == 8 ? launch_kernel(gate_kernel<1, 8>, dim3(grid), dim3(256), 0, s, a)
-                                        : launch_kernel(gate_kernel<1, 0>, dim3(grid), dim3(256), 0, s, a);
-            case 2: return a.top_k == 8 ? launch_kernel(gate_kernel<2, 8>, dim3(grid), dim3(256), 0, s, a)
-                                        : launch_kernel(gate_kernel<2, 0>, dim3(grid), dim3(256), 0, s, a);
-            case 4: return a.top_k == 8 ? launch_kernel(gate_kernel<4, 8>, dim3(grid), dim3(256), 0, s, a)
-                                        : launch_kernel(gate_kernel<4, 0>, dim3(grid), dim3(256), 0, s, a);
-            default: return a.top_k == 8 ? launch_kernel(gate_kernel<8, 8>, dim3(grid), dim3(256), 0, s, a)
-                                         : launch_kernel(gate_kernel<8, 0>, dim3(grid), dim3(256), 0, s, a);
+            case 1: if (k8) MOE_GATE(1, 8, 0); else MOE_GATE(1, 0, 0);
+            case 2: if (k8) MOE_GATE(2, 8, 0); else MOE_GATE(2, 0, 0);
+            case 4: if (k8) MOE_GATE(4, 8, 0); else MOE_GATE(4, 0, 0);
+            default: if (k8) MOE_GATE(8, 8, 0); else MOE_GATE(8, 0, 0);
         }
+#undef MOE_GATE
     }
     switch (epl) {
         case 1: return launch_kernel(route_kernel<1, false>, dim3(grid), dim3(256), 0, s, a);
