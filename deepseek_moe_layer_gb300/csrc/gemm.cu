@@ -430,7 +430,8 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
             // traffic of the launch 12.6 -> see the bench's traffic table)
             const uint64_t pol_w = C::kSwap ? policy_evict_first() : policy_evict_last();
             const uint64_t pol_x = policy_evict_last();
-            int it = 0;
+            int it = 0, s = 0;  // k-blocks issued; ring stage and its phase
+            uint32_t ph = 0u;
             bool ok = true;
             for (int t = tstart; t < total && ok; t += tstep) {
                 const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t, crank);
@@ -439,8 +440,7 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
                 const CUtensorMap* w1 = ti.shared ? &tm_sw1 : &tm_w1;
                 const int wrow = (ti.shared || !p.offsets ? 0 : ti.g * p.F) + ti.f * C::kFeat;
                 for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++it) {
-                    const int s = it % C::kStages;
-                    const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
+                    if (it > 0 && ++s == C::kStages) { s = 0; ph ^= 1u; }
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
                     uint8_t* st = smem + s * C::kStageBytes;
                     const int kx = kb * kBK;
@@ -494,7 +494,8 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
         // operand ring, so enough HBM reads stay in flight to stream the codes at full rate
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
-            int rit = 0;
+            int rit = 0, rs = 0;  // raw slots issued; raw ring slot and its phase
+            uint32_t rph = 0u;
             bool ok = true;
             for (int t = tstart; t < total && ok; t += tstep) {
                 const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t, crank);
@@ -503,8 +504,7 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
                     // TMEM-A path: one k-block of them per raw slot (same 128-byte rows)
                     if constexpr (C::kTA) {
                         for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++rit) {
-                            const int rs = rit % C::kRawRing;
-                            const uint32_t rph = (uint32_t)(rit / C::kRawRing) & 1u;
+                            if (rit > 0 && ++rs == C::kRawRing) { rs = 0; rph ^= 1u; }
                             if (!mbar_wait(&rawempty[rs], rph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
                             uint8_t* rst = smem + C::kRawOff + rs * C::kRBytes;
                             mbar_arrive_expect_tx(&rawfull[rs], C::kRBytes);
@@ -518,8 +518,7 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
                 }
                 const int wrow = ti.g * p.F + ti.f * C::kFeat;
                 for (int kb = ti.kb0; kb < ti.kb1; kb += C::kRawKB, ++rit) {
-                    const int rs = rit % C::kRawRing;
-                    const uint32_t rph = (uint32_t)(rit / C::kRawRing) & 1u;
+                    if (rit > 0 && ++rs == C::kRawRing) { rs = 0; rph ^= 1u; }
                     if (!mbar_wait(&rawempty[rs], rph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
                     uint8_t* rst = smem + C::kRawOff + rs * C::kRBytes;
                     mbar_arrive_expect_tx(&rawfull[rs], C::kRBytes);
@@ -543,7 +542,8 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
     } else if (warp == 1) {
         // ================================ UMMA issuer ===============================
         if (lane == 0) {
-            int it = 0, lt = 0;
+            int it = 0, lt = 0, s = 0;  // k-blocks consumed; ring stage and its phase
+            uint32_t ph = 0u;
             bool ok = true;
             for (int t = tstart; t < total && ok; t += tstep, ++lt) {
                 const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t, crank);
@@ -554,8 +554,7 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
                 tc_fence_after();
                 const uint32_t acc = tmem_base + (uint32_t)(ab * C::kAccCols);
                 for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++it) {
-                    const int s = it % C::kStages;
-                    const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
+                    if (it > 0 && ++s == C::kStages) { s = 0; ph ^= 1u; }
                     if (!(C::kPair ? mbar_wait_cluster(&full[s], ph, abort)
                                    : mbar_wait(&full[s], ph, abort))) { record_timeout(abort); ok = false; break; }
                     tc_fence_after();
@@ -638,11 +637,58 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
             const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
             return (unsigned short)((j & 1) ? (w >> 16) : (w & 0xFFFFu));
         };
-        int it = 0, rit = 0;  // operand-ring and raw-ring positions
+        // ring positions, advanced once per k-block (operand stage s, phase ph) and once per
+        // raw slot (rs, rph) in the order the producers and the MMA thread use them
+        int s = 0, rs = 0;
+        uint32_t ph = 0u, rph = 0u;
         bool ok = true;
         for (int t = tstart; t < total && ok; t += tstep) {
             const TileInfo ti = decode_tile<C>(p, prefix, rowoff, ngroups, t, crank);
-            const bool rvalid = !ti.shared && ti.f * C::kFeat + rr < p.F;
+            const uint32_t tcol0 = tmem_base + ((uint32_t)(qtr * 32) << 16) +
+                                   (uint32_t)(2 * C::kAccCols + (MODE == kGateUp ? half * 32 : 0) +
+                                              wd0 * 4);
+            if (ti.shared) {
+                // bf16 shared expert: its weight tile comes by TMA (normal path) or, on the
+                // TMEM-A path, one k-block per raw slot whose 128-byte rows are already the
+                // operand
+                for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
+                    uint4 bw[kWordsPT];
+                    if constexpr (C::kTA) {
+                        if (!mbar_wait(&rawfull[rs], rph, abort)) { record_timeout(abort); ok = false; break; }
+                        const uint8_t* rrow = smem + C::kRawOff + rs * C::kRBytes + r * 128;
+#pragma unroll
+                        for (int w = 0; w < kWordsPT; ++w)
+                            bw[w] = *reinterpret_cast<const uint4*>(rrow + (((wd0 + w) ^ (r & 7)) << 4));
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&rawempty[rs]);
+                        if (++rs == C::kRawRing) { rs = 0; rph ^= 1u; }
+                    }
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
+                    if constexpr (C::kTA) {
+                        tc_fence_after();
+                        const uint32_t tcol = tcol0 + (uint32_t)(s * C::kAStageCols);
+#pragma unroll
+                        for (int h = 0; h < kWordsPT / 4; ++h) {
+                            uint32_t v16[16];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                v16[4 * i] = bw[4 * h + i].x; v16[4 * i + 1] = bw[4 * h + i].y;
+                                v16[4 * i + 2] = bw[4 * h + i].z; v16[4 * i + 3] = bw[4 * h + i].w;
+                            }
+                            tmem_st16(tcol + (uint32_t)(16 * h), v16);
+                        }
+                        tmem_st_wait();
+                        tc_fence_before();
+                    } else {
+                        fence_proxy_async_smem();
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full[s]);
+                    if (++s == C::kStages) { s = 0; ph ^= 1u; }
+                }
+                continue;
+            }
+            const bool rvalid = ti.f * C::kFeat + rr < p.F;
             const long long grow = (long long)ti.g * p.F + ti.f * C::kFeat + rr;
             const unsigned short* srow = sp + grow * ngr;
             const unsigned short* brow = bp + grow * ngr;
@@ -656,103 +702,62 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
                     bc_nxt = __ldg(reinterpret_cast<const uint4*>(brow + wb + 8));
                 }
             }
-            for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++it) {
-                const int s = it % C::kStages;
-                const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
-                // the (at most two) groups of this thread's chunks in k-block kb
-                const int e0 = kb * kBK + 8 * wd0;
-                const int ga = e0 >> qsh, gb = (e0 + 8 * kWordsPT - 1) >> qsh;
-                unsigned short sa = 0, ba = 0, sb = 0, bb = 0;  // fp16 bits
-                if (vec) {
-                    if (ga >= wb + 8) {  // the groups advance by at most 2 per k-block
-                        sc_cur = sc_nxt;
-                        bc_cur = bc_nxt;
-                        wb += 8;
-                        if (rvalid && wb + 8 < ngr) {
-                            sc_nxt = __ldg(reinterpret_cast<const uint4*>(srow + wb + 8));
-                            bc_nxt = __ldg(reinterpret_cast<const uint4*>(brow + wb + 8));
+            // one raw slot (kRawKB k-blocks of this row's codes) per pass; the k-block within
+            // the slot is known at compile time
+            for (int kbs = ti.kb0; kbs < ti.kb1 && ok; kbs += C::kRawKB) {
+                if (!mbar_wait(&rawfull[rs], rph, abort)) { record_timeout(abort); ok = false; break; }
+                const uint8_t* rrow = smem + C::kRawOff + rs * C::kRBytes + r * 128;
+#pragma unroll
+                for (int j = 0; j < C::kRawKB; ++j) {
+                    const int kb = kbs + j;
+                    if (kb >= ti.kb1) break;
+                    // the (at most two) groups of this thread's chunks in k-block kb
+                    const int e0 = kb * kBK + 8 * wd0;
+                    const int ga = e0 >> qsh, gb = (e0 + 8 * kWordsPT - 1) >> qsh;
+                    unsigned short sa = 0, ba = 0, sb = 0, bb = 0;  // fp16 bits
+                    if (vec) {
+                        if (ga >= wb + 8) {  // the groups advance by at most 2 per k-block
+                            sc_cur = sc_nxt;
+                            bc_cur = bc_nxt;
+                            wb += 8;
+                            if (rvalid && wb + 8 < ngr) {
+                                sc_nxt = __ldg(reinterpret_cast<const uint4*>(srow + wb + 8));
+                                bc_nxt = __ldg(reinterpret_cast<const uint4*>(brow + wb + 8));
+                            }
                         }
+                        // both groups lie in the current window: windows start at multiples
+                        // of 8 groups and a split pair is (2m, 2m + 1) for 32-input groups.
+                        // The next window (still in flight) is only read at the slide above.
+                        const int ia = ga - wb, ib = gb - wb;
+                        sa = pick16(sc_cur, ia);
+                        ba = pick16(bc_cur, ia);
+                        sb = pick16(sc_cur, ib);
+                        bb = pick16(bc_cur, ib);
+                    } else if (rvalid) {
+                        sa = __ldg(srow + ga);
+                        ba = __ldg(brow + ga);
+                        sb = __ldg(srow + gb);
+                        bb = __ldg(brow + gb);
                     }
-                    // both groups lie in the current window: windows start at multiples of
-                    // 8 groups and a split pair is (2m, 2m + 1) for 32-input groups.  The
-                    // next window (still in flight) is only read at the slide above.
-                    const int ia = ga - wb, ib = gb - wb;
-                    sa = pick16(sc_cur, ia);
-                    ba = pick16(bc_cur, ia);
-                    sb = pick16(sc_cur, ib);
-                    bb = pick16(bc_cur, ib);
-                } else if (rvalid) {
-                    sa = __ldg(srow + ga);
-                    ba = __ldg(brow + ga);
-                    sb = __ldg(srow + gb);
-                    bb = __ldg(brow + gb);
-                }
-                uint32_t words[kWordsPT * kWPC];
-                if (!ti.shared) {
-                    // this row's codes of k-block kb from the current raw slot (a 128-byte
-                    // swizzled row segment of kRawKB k-blocks); the slot goes back to the
-                    // code producer after its last k-block
-                    const int j = (kb - ti.kb0) % C::kRawKB;
-                    const int rs = rit % C::kRawRing;
-                    if (j == 0) {
-                        const uint32_t rph = (uint32_t)(rit / C::kRawRing) & 1u;
-                        if (!mbar_wait(&rawfull[rs], rph, abort)) { record_timeout(abort); ok = false; break; }
-                    }
-                    const uint8_t* rrow = smem + C::kRawOff + rs * C::kRBytes + r * 128;
+                    // this row's codes of k-block kb: k-block j starts at byte 8 * QB * j of
+                    // the 128-byte swizzled row segment, chunk c at byte QB * c of the k-block
+                    uint32_t words[kWordsPT * kWPC];
 #pragma unroll
                     for (int v = 0; v < kPieces; ++v) {
-                        // k-block j starts at byte 8 * QB * j of the row segment, chunk c at
-                        // byte QB * c of the k-block
                         const int c16 = j * QB / 2 + wd0 * QB / 16 + v;
-                        const uint4 q4 =
-                            *reinterpret_cast<const uint4*>(rrow + ((c16 ^ (r & 7)) << 4));
+                        const uint4 q4 = *reinterpret_cast<const uint4*>(rrow + ((c16 ^ (r & 7)) << 4));
                         words[4 * v] = q4.x; words[4 * v + 1] = q4.y;
                         words[4 * v + 2] = q4.z; words[4 * v + 3] = q4.w;
                     }
                     if (j == C::kRawKB - 1 || kb + 1 == ti.kb1) {
+                        // the slot goes back to the code producer after its last k-block
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&rawempty[rs]);
-                        ++rit;
+                        if (++rs == C::kRawRing) { rs = 0; rph ^= 1u; }
                     }
-                } else if (C::kTA) {
-                    // bf16 shared expert on the TMEM-A path: one k-block per raw slot, the
-                    // row's 128 bytes are already the operand
-                    const int rs = rit % C::kRawRing;
-                    const uint32_t rph = (uint32_t)(rit / C::kRawRing) & 1u;
-                    if (!mbar_wait(&rawfull[rs], rph, abort)) { record_timeout(abort); ok = false; break; }
-                    const uint8_t* rrow = smem + C::kRawOff + rs * C::kRBytes + r * 128;
-                    uint4 bw[kWordsPT];
-#pragma unroll
-                    for (int w = 0; w < kWordsPT; ++w)
-                        bw[w] = *reinterpret_cast<const uint4*>(rrow + (((wd0 + w) ^ (r & 7)) << 4));
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&rawempty[rs]);
-                    ++rit;
-                    if (!mbar_wait(&empty[s], ph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t tcol = tmem_base + ((uint32_t)(qtr * 32) << 16) +
-                                          (uint32_t)(2 * C::kAccCols + s * C::kAStageCols +
-                                                     (MODE == kGateUp ? half * 32 : 0) + wd0 * 4);
-#pragma unroll
-                    for (int h = 0; h < kWordsPT / 4; ++h) {
-                        uint32_t v16[16];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            v16[4 * i] = bw[4 * h + i].x; v16[4 * i + 1] = bw[4 * h + i].y;
-                            v16[4 * i + 2] = bw[4 * h + i].z; v16[4 * i + 3] = bw[4 * h + i].w;
-                        }
-                        tmem_st16(tcol + (uint32_t)(16 * h), v16);
-                    }
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&full[s]);
-                    continue;
-                }
-                // dequantise into registers first, so the math overlaps the wait for the
-                // operand slot (free once the MMA has consumed its previous contents)
-                uint4 dq8[kWordsPT];
-                if (!ti.shared) {
+                    // dequantise into registers first, so the math overlaps the wait for the
+                    // operand slot (free once the MMA has consumed its previous contents)
+                    uint4 dq8[kWordsPT];
                     const float sfa = __half2float(__ushort_as_half(sa));
                     const float bfa = __half2float(__ushort_as_half(ba));
                     if constexpr (QG != 32) {  // one group for all of this thread's chunks
@@ -773,39 +778,36 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
                                              : dequant8_u8(words[2 * w], words[2 * w + 1], sf, bf);
                         }
                     }
-                }
-                if (!mbar_wait(&empty[s], ph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
-                if (C::kTA) {
-                    // weights -> this stage's TMEM columns of the warp's lane quarter
-                    tc_fence_after();
-                    const uint32_t tcol = tmem_base + ((uint32_t)(qtr * 32) << 16) +
-                                          (uint32_t)(2 * C::kAccCols + s * C::kAStageCols +
-                                                     (MODE == kGateUp ? half * 32 : 0) + wd0 * 4);
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort)) { record_timeout(abort); ok = false; break; }
+                    if constexpr (C::kTA) {
+                        // weights -> this stage's TMEM columns of the warp's lane quarter
+                        tc_fence_after();
+                        const uint32_t tcol = tcol0 + (uint32_t)(s * C::kAStageCols);
 #pragma unroll
-                    for (int h = 0; h < kWordsPT / 4; ++h) {
-                        uint32_t v16[16];
+                        for (int h = 0; h < kWordsPT / 4; ++h) {
+                            uint32_t v16[16];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            v16[4 * i] = dq8[4 * h + i].x; v16[4 * i + 1] = dq8[4 * h + i].y;
-                            v16[4 * i + 2] = dq8[4 * h + i].z; v16[4 * i + 3] = dq8[4 * h + i].w;
+                            for (int i = 0; i < 4; ++i) {
+                                v16[4 * i] = dq8[4 * h + i].x; v16[4 * i + 1] = dq8[4 * h + i].y;
+                                v16[4 * i + 2] = dq8[4 * h + i].z; v16[4 * i + 3] = dq8[4 * h + i].w;
+                            }
+                            tmem_st16(tcol + (uint32_t)(16 * h), v16);
                         }
-                        tmem_st16(tcol + (uint32_t)(16 * h), v16);
-                    }
-                    tmem_st_wait();
-                    tc_fence_before();
-                } else {
-                    if (!ti.shared) {
+                        tmem_st_wait();
+                        tc_fence_before();
+                    } else {
                         uint8_t* wrow_s = smem + s * C::kStageBytes + C::kXBytes + r * 128;
 #pragma unroll
                         for (int w = 0; w < kWordsPT; ++w) {
                             const int c = wd0 + w;  // 16-byte chunk = 8 elements of the row
                             *reinterpret_cast<uint4*>(wrow_s + ((c ^ (r & 7)) << 4)) = dq8[w];
                         }
+                        fence_proxy_async_smem();
                     }
-                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full[s]);
+                    if (++s == C::kStages) { s = 0; ph ^= 1u; }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full[s]);
             }
         }
     } else {
