@@ -208,6 +208,25 @@ MOE_DEV uint4 dequant8_u8(uint32_t w0, uint32_t w1, float sc, float bi) {
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// The GPS consecutive 16-bit values of an 8-value window v that start at `off` (a multiple
+// of GPS), two per word: values 2i and 2i+1 in the low and high half of out[i].
+template <int GPS>
+MOE_DEV void window_part(const uint4& v, int off, uint32_t (&out)[(GPS + 1) / 2]) {
+    if constexpr (GPS == 8) {
+        out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+    } else if constexpr (GPS == 4) {
+        const bool h = off >= 4;
+        out[0] = h ? v.z : v.x;
+        out[1] = h ? v.w : v.y;
+    } else if constexpr (GPS == 2) {
+        const int q = off >> 1;
+        out[0] = q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+    } else {
+        const uint32_t w = off < 2 ? v.x : off < 4 ? v.y : off < 6 ? v.z : v.w;
+        out[0] = (off & 1) ? (w >> 16) : (w & 0xFFFFu);
+    }
+}
+
 // Staged epilogue stores.  A warp's 32 accumulator rows (one per lane) are written to a
 // shared buffer of 32 rows x COLS bf16 as 16-byte chunks, then read back with COLS/8 lanes per
 // row so that each warp store covers whole row segments (a 128-byte line for 64 columns, half
@@ -703,10 +722,30 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
                 }
             }
             // one raw slot (kRawKB k-blocks of this row's codes) per pass; the k-block within
-            // the slot is known at compile time
+            // the slot is known at compile time.  When the thread's chunks start its rows'
+            // k-blocks and the tile starts on a slot boundary, a slot's groups are a fixed part
+            // of the 8-group scale window, taken once per slot; each k-block then reads its
+            // group's scale and bias at a compile-time position.
+            constexpr int kGPS = QG ? C::kRawKB * kBK / QG : 1;  // scale groups per raw slot
+            const bool slot_win = vec && wd0 == 0 && ti.kb0 % C::kRawKB == 0;
             for (int kbs = ti.kb0; kbs < ti.kb1 && ok; kbs += C::kRawKB) {
                 if (!mbar_wait(&rawfull[rs], rph, abort)) { record_timeout(abort); ok = false; break; }
                 const uint8_t* rrow = smem + C::kRawOff + rs * C::kRBytes + r * 128;
+                uint32_t sgw[(kGPS + 1) / 2], bgw[(kGPS + 1) / 2];
+                if (slot_win) {
+                    const int gs = (kbs * kBK) >> qsh;
+                    if (gs >= wb + 8) {  // slots advance by kGPS groups, which divides 8
+                        sc_cur = sc_nxt;
+                        bc_cur = bc_nxt;
+                        wb += 8;
+                        if (rvalid && wb + 8 < ngr) {
+                            sc_nxt = __ldg(reinterpret_cast<const uint4*>(srow + wb + 8));
+                            bc_nxt = __ldg(reinterpret_cast<const uint4*>(brow + wb + 8));
+                        }
+                    }
+                    window_part<kGPS>(sc_cur, gs - wb, sgw);
+                    window_part<kGPS>(bc_cur, gs - wb, bgw);
+                }
 #pragma unroll
                 for (int j = 0; j < C::kRawKB; ++j) {
                     const int kb = kbs + j;
@@ -715,7 +754,15 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
                     const int e0 = kb * kBK + 8 * wd0;
                     const int ga = e0 >> qsh, gb = (e0 + 8 * kWordsPT - 1) >> qsh;
                     unsigned short sa = 0, ba = 0, sb = 0, bb = 0;  // fp16 bits
-                    if (vec) {
+                    if (slot_win) {
+                        // groups j*kBK/QG and (j*kBK + kBK-1)/QG of the slot
+                        const int ia = QG ? (j * kBK) / QG : 0;
+                        const int ib = QG ? (j * kBK + kBK - 1) / QG : 0;
+                        sa = (unsigned short)(sgw[ia / 2] >> (16 * (ia & 1)));
+                        ba = (unsigned short)(bgw[ia / 2] >> (16 * (ia & 1)));
+                        sb = (unsigned short)(sgw[ib / 2] >> (16 * (ib & 1)));
+                        bb = (unsigned short)(bgw[ib / 2] >> (16 * (ib & 1)));
+                    } else if (vec) {
                         if (ga >= wb + 8) {  // the groups advance by at most 2 per k-block
                             sc_cur = sc_nxt;
                             bc_cur = bc_nxt;
