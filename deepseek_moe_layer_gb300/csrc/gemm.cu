@@ -579,34 +579,33 @@ __global__ void __launch_bounds__(Cfg<MODE, TOKT, QB, PAIR>::kThreadsCta, 1)
                     tc_fence_after();
                     const uint32_t xs = smem_u32(smem + s * C::kStageBytes);
                     const uint32_t ws = xs + C::kXBytes;
+                    // the stage's operand descriptors, once; a K = 16 step is 32 bytes further
+                    // (2 in the address field, which holds any shared-memory address)
+                    const uint64_t dx = sdesc_k128(xs), dw = sdesc_k128(ws);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint32_t accum = (kb > ti.kb0 || kk > 0) ? 1u : 0u;
+                        const uint64_t dxk = dx + (uint64_t)(2 * kk), dwk = dw + (uint64_t)(2 * kk);
                         if (C::kTA) {
                             // A (weights) from this stage's TMEM columns, 8 per K=16 slice
-                            const uint64_t bd = sdesc_k128(xs + kk * 32);
                             const uint32_t a0 = tmem_base + (uint32_t)(2 * C::kAccCols +
                                                                        s * C::kAStageCols + kk * 8);
 #pragma unroll
                             for (int w = 0; w < C::kNW; ++w)
                                 umma_bf16_ta(acc + (uint32_t)(w * C::kTok),
-                                             a0 + (uint32_t)(w * 32), bd, C::kIdesc, accum);
+                                             a0 + (uint32_t)(w * 32), dxk, C::kIdesc, accum);
                         } else if (C::kSwap) {
-                            const uint64_t bd = sdesc_k128(xs + kk * 32);
 #pragma unroll
                             for (int w = 0; w < C::kNW; ++w)
                                 umma_bf16(acc + (uint32_t)(w * C::kTok),
-                                          sdesc_k128(ws + w * 128 * 128 + kk * 32), bd,
-                                          C::kIdesc, accum);
+                                          dwk + (uint64_t)(w * 128 * 128 / 16), dxk, C::kIdesc, accum);
                         } else if (C::kPair) {
-                            umma_bf16_pair(acc, sdesc_k128(xs + kk * 32), sdesc_k128(ws + kk * 32),
-                                           C::kIdesc, accum);
+                            umma_bf16_pair(acc, dxk, dwk, C::kIdesc, accum);
                         } else {
-                            const uint64_t bd = sdesc_k128(ws + kk * 32);
-                            umma_bf16(acc, sdesc_k128(xs + kk * 32), bd, C::kIdesc, accum);
+                            umma_bf16(acc, dxk, dwk, C::kIdesc, accum);
                             // the second sub-tile's tokens, when the tile has any
                             if (C::kM2 && ti.rows > 128)
-                                umma_bf16(acc + 256u, sdesc_k128(xs + 128 * 128 + kk * 32), bd,
+                                umma_bf16(acc + 256u, dxk + (uint64_t)(128 * 128 / 16), dwk,
                                           C::kIdesc, accum);
                         }
                     }
