@@ -41,10 +41,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # workloads (routing is deterministic, so a launch's traffic is fixed), keyed by workload
 # with the hash of the GEMM sources the capture ran; a stale hash reports null.
 NCU_TRAFFIC = {
-    "dsv3_T128": {"src": "1dce7837455b4984", "ratio": 4613574741 / 4601413632},
-    "dsv3_T8192_zipf": {"src": "1dce7837455b4984", "ratio": 10456219648 / 7935623168},
-    "dsv3_q4_T32": {"src": "1dce7837455b4984", "ratio": 961202176 / 922812416},
-    "dsv3_q8_T32": {"src": "1dce7837455b4984", "ratio": 1739855190 / 1686175744},
+    "dsv3_T128": {"src": "766546b89d3431a7", "ratio": 4619120854 / 4601413632},
+    "dsv3_T8192_zipf": {"src": "766546b89d3431a7", "ratio": 10454055765 / 7935623168},
+    "dsv3_q4_T32": {"src": "766546b89d3431a7", "ratio": 961363115 / 922812416},
+    "dsv3_q8_T32": {"src": "766546b89d3431a7", "ratio": 1743873238 / 1686175744},
+    "dsv3_q4_T4096_zipf": {"src": "766546b89d3431a7", "ratio": 3130795051 / 2521825280},
+    "dsv3_q8_T4096_zipf": {"src": "766546b89d3431a7", "ratio": 5094885461 / 4107272192},
 }
 
 
